@@ -1,0 +1,183 @@
+"""ctypes wrapper around the fp64 C oracle (``oracle/oracle.c``).
+
+TEST INFRASTRUCTURE ONLY.  Only the test suite, ``__graft_entry__.smoke()`` and
+the benchmark's CPU-baseline leg import this package.  It never touches the
+CUDA library and the CUDA library never touches it.
+
+The shared object is built with gcc into ``oracle/_build/liboracle.so`` on
+first use (or by ``__graft_entry__.build()``).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_OUT_DIR = os.path.join(_HERE, "_build")
+_SO = os.path.join(_OUT_DIR, "liboracle.so")
+
+ORC_OK = 0
+ORC_BAD_VALUE = -1
+ORC_BAD_SHAPE = -2
+ORC_BAD_CODE = -3
+
+_lib = None
+_lock = threading.Lock()
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (plain -O2, no vectorisation flags)."""
+    os.makedirs(_OUT_DIR, exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            i64, p = ctypes.c_int64, ctypes.c_void_p
+            lib.orc_pack.argtypes = [p, i64, i64, p]
+            lib.orc_unpack.argtypes = [p, i64, i64, p]
+            lib.orc_stats.argtypes = [p, i64, i64, p, p]
+            lib.orc_gemm.argtypes = [p, p, i64, i64, p, i64, p, i64, i64]
+            lib.orc_swiglu.argtypes = [p, p, p, p, i64, i64, p, i64, p, i64, i64]
+            lib.orc_silu.argtypes = [ctypes.c_double]
+            lib.orc_silu.restype = ctypes.c_double
+            lib.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
+            lib.orc_bf16_to_double.restype = ctypes.c_double
+            for f in (lib.orc_pack, lib.orc_unpack, lib.orc_stats, lib.orc_gemm, lib.orc_swiglu):
+                f.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def _check(rc: int, what: str):
+    if rc != ORC_OK:
+        raise OracleError(f"{what}: oracle status {rc}")
+
+
+def pack(t: np.ndarray) -> np.ndarray:
+    """int8 [rows, k] -> uint32 [rows, k//16] in the project's 2-bit format."""
+    t = np.ascontiguousarray(t, dtype=np.int8)
+    rows, k = t.shape
+    codes = np.zeros((rows, k // 16 if k % 64 == 0 else 0), dtype=np.uint32)
+    _check(_load().orc_pack(_ptr(t), rows, k, _ptr(codes)), "pack")
+    return codes
+
+
+def unpack(codes: np.ndarray, k: int) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.uint32)
+    rows = codes.shape[0]
+    t = np.zeros((rows, k), dtype=np.int8)
+    _check(_load().orc_unpack(_ptr(codes), rows, k, _ptr(t)), "unpack")
+    return t
+
+
+def stats(codes: np.ndarray, k: int):
+    """Returns (rowsum int64 [rows], counts int64 [3] = zeros, plus, minus)."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint32)
+    rows = codes.shape[0]
+    rowsum = np.zeros(rows, dtype=np.int64)
+    counts = np.zeros(3, dtype=np.int64)
+    _check(_load().orc_stats(_ptr(codes), rows, k, _ptr(rowsum), _ptr(counts)), "stats")
+    return rowsum, counts
+
+
+def _row_split(rows: int, threads: int):
+    threads = max(1, min(threads, rows)) if rows > 0 else 1
+    step = (rows + threads - 1) // threads if rows > 0 else 0
+    return [(b, min(rows, b + step)) for b in range(0, rows, step)] if rows > 0 else []
+
+
+def _run_rows(fn, rows: int, threads: int, rows_subset=None):
+    """Run fn(row_begin, row_end) over row ranges on Python threads.
+
+    ctypes releases the GIL during the C call, so the ranges run in parallel.
+    ``rows_subset`` (sorted row indices) restricts the work to those rows.
+    """
+    if rows_subset is not None:
+        ranges = [(int(r), int(r) + 1) for r in rows_subset]
+    else:
+        ranges = _row_split(rows, threads)
+    errs = []
+
+    def worker(chunk):
+        for (b, e) in chunk:
+            rc = fn(b, e)
+            if rc != ORC_OK:
+                errs.append(rc)
+                return
+
+    nthreads = max(1, min(threads, len(ranges)))
+    chunks = [ranges[i::nthreads] for i in range(nthreads)]
+    if nthreads == 1:
+        worker(chunks[0] if chunks else [])
+    else:
+        ts = [threading.Thread(target=worker, args=(c,)) for c in chunks]
+        for th in ts:
+            th.start()
+        for th in ts:
+            th.join()
+    if errs:
+        raise OracleError(f"oracle status {errs[0]}")
+
+
+def gemm(codes: np.ndarray, scale: np.ndarray, k: int, x_bits: np.ndarray,
+         threads: int = 1, rows_subset=None) -> np.ndarray:
+    """y [m, rows] float64 = scale * (T @ x), x given as bf16 bits [m, k]."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint32)
+    scale = np.ascontiguousarray(scale, dtype=np.float32)
+    x_bits = np.ascontiguousarray(np.atleast_2d(x_bits), dtype=np.uint16)
+    rows = codes.shape[0]
+    m = x_bits.shape[0]
+    assert x_bits.shape[1] == k
+    y = np.zeros((m, rows), dtype=np.float64)
+    lib = _load()
+    _run_rows(lambda b, e: lib.orc_gemm(_ptr(codes), _ptr(scale), rows, k, _ptr(x_bits), m,
+                                        _ptr(y), b, e), rows, threads, rows_subset)
+    return y
+
+
+def swiglu(g_codes, g_scale, u_codes, u_scale, k: int, x_bits: np.ndarray,
+           threads: int = 1, rows_subset=None) -> np.ndarray:
+    """h [m, rows] float64 = silu(g) * u."""
+    g_codes = np.ascontiguousarray(g_codes, dtype=np.uint32)
+    u_codes = np.ascontiguousarray(u_codes, dtype=np.uint32)
+    g_scale = np.ascontiguousarray(g_scale, dtype=np.float32)
+    u_scale = np.ascontiguousarray(u_scale, dtype=np.float32)
+    x_bits = np.ascontiguousarray(np.atleast_2d(x_bits), dtype=np.uint16)
+    rows = g_codes.shape[0]
+    assert u_codes.shape == g_codes.shape
+    m = x_bits.shape[0]
+    h = np.zeros((m, rows), dtype=np.float64)
+    lib = _load()
+    _run_rows(lambda b, e: lib.orc_swiglu(_ptr(g_codes), _ptr(g_scale), _ptr(u_codes), _ptr(u_scale),
+                                          rows, k, _ptr(x_bits), m, _ptr(h), b, e),
+              rows, threads, rows_subset)
+    return h
+
+
+def silu(z: float) -> float:
+    return _load().orc_silu(float(z))
+
+
+def bf16_to_double(bits: int) -> float:
+    return _load().orc_bf16_to_double(int(bits))

@@ -1,0 +1,182 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle for the ternary linear layer.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file: only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header, table or constant with
+ * the CUDA library; it decodes the packed format with its own decoder written
+ * from the format definition below.
+ *
+ * What it computes (Neutrino-1 8B model page, intro: every transformer linear
+ * is stored bit-packed and decoded inside the matrix kernels; spec table:
+ * gated (SwiGLU) feed-forward, three linears per layer; "Where the bytes
+ * live": per-row metadata holds row dimensions, scales and row sums):
+ *
+ *   y[m][r] = scale[r] * sum_k t[r][k] * x[m][k]          t in {-1, 0, +1}
+ *   h[m][r] = silu(g[m][r]) * u[m][r],  silu(z) = z / (1 + exp(-z))
+ *   rowsum[r] = sum_k t[r][k]
+ *
+ * The page calls its real bit format proprietary and never specifies it, so
+ * the format decoded here is this project's own 2-bit format:
+ *   - a matrix of R rows and K columns (K a multiple of 64) is R*K/16 uint32
+ *     words, row-major, K-contiguous: row r owns words [r*K/16, (r+1)*K/16);
+ *   - column k of row r lives in word r*K/16 + k/16, at bits 2*(k%16) (low,
+ *     "b0") and 2*(k%16)+1 (high, "b1"), least significant code first;
+ *   - (b1,b0) = 00 -> 0, 01 -> +1, 11 -> -1; 10 is invalid.
+ *
+ * Arithmetic: every activation is widened from bf16 to double exactly, every
+ * product t*x is exact, the sum over k runs in increasing k in double, and the
+ * fp32 scale is applied in double.  No blocking, no reordering.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stddef.h>
+
+#define ORC_OK 0
+#define ORC_BAD_VALUE (-1) /* int8 weight outside {-1,0,+1} */
+#define ORC_BAD_SHAPE (-2) /* K not a multiple of 64, or negative sizes */
+#define ORC_BAD_CODE (-3)  /* a 2-bit field holds the invalid pattern 10 */
+
+/* Value of one 2-bit field, or 2 for the invalid pattern. */
+static int orc_field_value(unsigned field)
+{
+    switch (field & 3u) {
+    case 0u: return 0;
+    case 1u: return 1;
+    case 3u: return -1;
+    default: return 2;
+    }
+}
+
+/* The 2-bit field holding column k of row r. */
+static unsigned orc_field(const uint32_t *codes, int64_t k_total, int64_t r, int64_t k)
+{
+    const int64_t words_per_row = k_total / 16;
+    const uint32_t w = codes[r * words_per_row + k / 16];
+    return (unsigned)((w >> (2 * (k % 16))) & 3u);
+}
+
+double orc_bf16_to_double(uint16_t bits)
+{
+    union { uint32_t u; float f; } v;
+    v.u = (uint32_t)bits << 16;
+    return (double)v.f;
+}
+
+/* Encode int8 weights into the 2-bit format.  Returns ORC_OK or an error. */
+int orc_pack(const int8_t *t, int64_t rows, int64_t k, uint32_t *codes)
+{
+    if (rows < 0 || k < 0 || k % 64 != 0) return ORC_BAD_SHAPE;
+    const int64_t wpr = k / 16;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t i = 0; i < wpr; ++i) {
+            uint32_t w = 0;
+            for (int64_t j = 0; j < 16; ++j) {
+                const int v = t[r * k + i * 16 + j];
+                uint32_t field;
+                if (v == 0) field = 0u;
+                else if (v == 1) field = 1u;
+                else if (v == -1) field = 3u;
+                else return ORC_BAD_VALUE;
+                w |= field << (2 * j);
+            }
+            codes[r * wpr + i] = w;
+        }
+    }
+    return ORC_OK;
+}
+
+/* Decode the whole matrix back to int8.  Returns ORC_OK or ORC_BAD_CODE. */
+int orc_unpack(const uint32_t *codes, int64_t rows, int64_t k, int8_t *t)
+{
+    if (rows < 0 || k < 0 || k % 64 != 0) return ORC_BAD_SHAPE;
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t c = 0; c < k; ++c) {
+            const int v = orc_field_value(orc_field(codes, k, r, c));
+            if (v == 2) return ORC_BAD_CODE;
+            t[r * k + c] = (int8_t)v;
+        }
+    }
+    return ORC_OK;
+}
+
+/*
+ * Per-row sums and code counts.  rowsum[r] = sum_k t[r][k] (int64 here; the
+ * stored metadata is int32), counts = {zeros, plus, minus} over the matrix.
+ */
+int orc_stats(const uint32_t *codes, int64_t rows, int64_t k,
+              int64_t *rowsum, int64_t counts[3])
+{
+    if (rows < 0 || k < 0 || k % 64 != 0) return ORC_BAD_SHAPE;
+    counts[0] = counts[1] = counts[2] = 0;
+    for (int64_t r = 0; r < rows; ++r) {
+        int64_t s = 0;
+        for (int64_t c = 0; c < k; ++c) {
+            const int v = orc_field_value(orc_field(codes, k, r, c));
+            if (v == 2) return ORC_BAD_CODE;
+            s += v;
+            counts[v == 0 ? 0 : (v == 1 ? 1 : 2)] += 1;
+        }
+        rowsum[r] = s;
+    }
+    return ORC_OK;
+}
+
+/*
+ * y[mi*rows + r] = scale[r] * sum_k t[r][k] * x[mi*k + k']  for rows in
+ * [row_begin, row_end) and every activation row mi < m.  x holds bf16 bit
+ * patterns.  An invalid field aborts with ORC_BAD_CODE.
+ */
+int orc_gemm(const uint32_t *codes, const float *scale, int64_t rows, int64_t k,
+             const uint16_t *x, int64_t m, double *y,
+             int64_t row_begin, int64_t row_end)
+{
+    if (rows < 0 || k < 0 || k % 64 != 0 || m < 0) return ORC_BAD_SHAPE;
+    for (int64_t mi = 0; mi < m; ++mi) {
+        for (int64_t r = row_begin; r < row_end; ++r) {
+            double acc = 0.0;
+            for (int64_t c = 0; c < k; ++c) {
+                const int v = orc_field_value(orc_field(codes, k, r, c));
+                if (v == 2) return ORC_BAD_CODE;
+                acc += (double)v * orc_bf16_to_double(x[mi * k + c]);
+            }
+            y[mi * rows + r] = (double)scale[r] * acc;
+        }
+    }
+    return ORC_OK;
+}
+
+/* silu(z) = z * sigmoid(z) = z / (1 + exp(-z)), in double. */
+double orc_silu(double z)
+{
+    return z / (1.0 + exp(-z));
+}
+
+/*
+ * Gated feed-forward activation: h = silu(gate) * up, where gate and up are
+ * the two projections of the same activations, each with its own scale.
+ */
+int orc_swiglu(const uint32_t *gate_codes, const float *gate_scale,
+               const uint32_t *up_codes, const float *up_scale,
+               int64_t rows, int64_t k, const uint16_t *x, int64_t m, double *h,
+               int64_t row_begin, int64_t row_end)
+{
+    if (rows < 0 || k < 0 || k % 64 != 0 || m < 0) return ORC_BAD_SHAPE;
+    for (int64_t mi = 0; mi < m; ++mi) {
+        for (int64_t r = row_begin; r < row_end; ++r) {
+            double g = 0.0, u = 0.0;
+            for (int64_t c = 0; c < k; ++c) {
+                const int vg = orc_field_value(orc_field(gate_codes, k, r, c));
+                const int vu = orc_field_value(orc_field(up_codes, k, r, c));
+                if (vg == 2 || vu == 2) return ORC_BAD_CODE;
+                const double xv = orc_bf16_to_double(x[mi * k + c]);
+                g += (double)vg * xv;
+                u += (double)vu * xv;
+            }
+            g *= (double)gate_scale[r];
+            u *= (double)up_scale[r];
+            h[mi * rows + r] = orc_silu(g) * u;
+        }
+    }
+    return ORC_OK;
+}
