@@ -1,0 +1,436 @@
+#!/usr/bin/env python3
+"""Benchmark of the ternary packed-weight GEMV on one or more GPUs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c1] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  Metric: packed-weight GB/s at M=1 (and
+microseconds per call), as a fraction of the measured HBM peak.
+
+Workloads (seeded synthetic inputs, shapes of the Neutrino-1 8B linears):
+  c0  M=1 GEMV 1024x4096            c1  M=1 GEMV 4096x4096 (default)
+  c2  M=1 down 4096x12288 + fused gate/up 2x12288x4096 (SiLU(g)*u)
+  c3  M=7 gate/up (fused) + down    c4  36-layer sweep, 252 linears per step
+
+One step is one pass over the workload's calls.  c0-c3 rotate over distinct
+device buffers holding more than three times the 126 MB L2 of packed weights,
+so every call streams from HBM; the calls of one step are captured once in a
+CUDA graph and replayed.  ``--impl reference`` times the fp64 CPU oracle on
+the host cores instead (a deliberately slow baseline).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "packed-weight GB/s and µs/call at M=1 (fraction of B300 HBM peak)"
+FALLBACK_HBM_GBS = 6400.0
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=100)
+    ap.add_argument("--workload", default="c1", choices=["c0", "c1", "c2", "c3", "c4"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas: each rank runs its own independent batch)
+# ---------------------------------------------------------------------------
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, v: float) -> float:
+        return reduce_max(self.pg, v)
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+def reduce_max(dist, v: float) -> float:
+    """Max of a float over all ranks (identity without a process group)."""
+    if dist is None:
+        return v
+    import torch
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [s.strip() for s in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# ncu traffic summary (per launch), valid only while the kernel source is unchanged
+# ---------------------------------------------------------------------------
+def kernel_source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "packed_bit_gemv_tern_b300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, fn), "rb") as f:
+                h.update(fn.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None, None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("source_digest") != kernel_source_digest():
+        return None, None
+    return e.get("dram_bytes_per_launch"), e.get("kernel")
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle baseline
+# ---------------------------------------------------------------------------
+def oracle_sample_rate(wl, budget_s: float, threads: int):
+    """Time the fp64 oracle over a bounded sample of the workload's calls.
+
+    Returns (packed GB/s, packed bytes processed, seconds, description).
+    The sample walks the calls in order, each call over a slice of its rows,
+    until ``budget_s`` of wall time has been spent.
+    """
+    import oracle
+    done_bytes, t0, ncalls, nrows = 0, time.perf_counter(), 0, 0
+    packed = getattr(wl, "_oracle_packed", None)
+    if packed is None:
+        packed = {}
+        for h in wl.host:
+            for lin in (h["lin"], h.get("up")):
+                if lin is not None and id(lin) not in packed:
+                    packed[id(lin)] = oracle.pack(lin.t)
+        wl._oracle_packed = packed
+    t0 = time.perf_counter()
+    while True:
+        for c, h in zip(wl.calls, wl.host):
+            lin = h["lin"]
+            rows = min(lin.rows, max(threads * 16, 256))
+            if "up" in h:
+                _oracle_swiglu_rows(oracle, packed, lin, h, rows, threads)
+                done_bytes += 2 * rows * lin.k // 4
+            else:
+                _oracle_gemm_rows(oracle, packed[id(lin)], lin, h["x_bits"], rows, threads)
+                done_bytes += rows * lin.k // 4
+            ncalls += 1
+            nrows += rows
+            if time.perf_counter() - t0 >= budget_s:
+                dt = time.perf_counter() - t0
+                desc = (f"{ncalls} calls of workload {wl.name}, first {nrows // max(ncalls, 1)} rows of each "
+                        f"(all K columns), {done_bytes / 1e6:.1f} MB of packed weights")
+                return done_bytes / dt / 1e9, done_bytes, dt, desc
+
+
+def _oracle_gemm_rows(oracle, codes, lin, x_bits, rows, threads):
+    oracle.gemm(codes[:rows], lin.scale[:rows], lin.k, x_bits, threads=threads)
+
+
+def _oracle_swiglu_rows(oracle, packed, lin, h, r, threads):
+    oracle.swiglu(packed[id(lin)][:r], lin.scale[:r], packed[id(h["up"])][:r], h["up"].scale[:r], lin.k,
+                  h["x_bits"], threads=threads)
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+def run_reference(args, dist: Dist):
+    """Reference arm: the fp64 CPU oracle as it stands, on the host cores."""
+    if dist.rank != 0:
+        return 0
+    from packed_bit_gemv_tern_b300 import synth, workloads  # noqa: F401
+    wl = _host_only_workload(args.workload)
+    threads = os.cpu_count() or 1
+    per_step_budget = max(0.002, min(1.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample_rate(wl, per_step_budget, threads)
+    tot_bytes, tot_s = 0, 0.0
+    desc = ""
+    for _ in range(args.steps):
+        _, b, dt, desc = oracle_sample_rate(wl, per_step_budget, threads)
+        tot_bytes += b
+        tot_s += dt
+    gbs = tot_bytes / tot_s / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot_s / max(1, args.steps), 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: {wl.desc}"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"per step ~{per_step_budget:.3f} s: {desc}"},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+class _HostWL:
+    def __init__(self, name, desc):
+        self.name, self.desc, self.calls, self.host = name, desc, [], []
+
+
+def _host_only_workload(name):
+    """Host copies of one unit of a workload (no GPU), for the oracle arm."""
+    from packed_bit_gemv_tern_b300 import synth
+    spec = synth.WORKLOADS[name]
+    rng = np.random.default_rng(spec["seed"])
+    wl = _HostWL(name, spec["desc"])
+    if name in ("c0", "c1"):
+        rows = 1024 if name == "c0" else 4096
+        lin = synth.linear(rng, rows, 4096)
+        wl.calls.append(None)
+        wl.host.append(dict(lin=lin, x_bits=synth.activations(rng, 1, 4096)))
+    elif name in ("c2", "c3"):
+        m = 1 if name == "c2" else 7
+        pz = 0.71 if name == "c2" else synth.P_ZERO
+        gate = synth.linear(rng, 12288, 4096, p_zero=pz)
+        up = synth.linear(rng, 12288, 4096, p_zero=pz)
+        down = synth.linear(rng, 4096, 12288, p_zero=pz)
+        wl.calls += [None, None]
+        wl.host.append(dict(lin=gate, up=up, x_bits=synth.activations(rng, m, 4096)))
+        wl.host.append(dict(lin=down, x_bits=synth.activations(rng, m, 12288)))
+    else:
+        for lname, rows, k in synth.LAYER_LINEARS:
+            lin = synth.linear(rng, rows, k, p_zero=synth.sweep_zero_fraction(0, lname))
+            wl.calls.append(None)
+            wl.host.append(dict(lin=lin, x_bits=synth.activations(rng, 1, k)))
+    return wl
+
+
+def run_ours(args, dist: Dist):
+    import torch
+
+    import packed_bit_gemv_tern_b300 as tern
+    from packed_bit_gemv_tern_b300 import workloads
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU for --impl ours")
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    tern.load()
+    wl = workloads.build(args.workload, device=dev, seed_offset=dist.rank)
+    ncalls = len(wl.calls)
+    stream = torch.cuda.Stream(device=dev)
+
+    # one eager pass (sets kernel attributes), then capture the step in a graph
+    with torch.cuda.stream(stream):
+        workloads.run_calls(wl.calls, stream)
+    stream.synchronize()
+    if tern.tern_last_device_error(stream) != tern.TERN_OK:
+        raise SystemExit("device error after the first pass")
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        workloads.run_calls(wl.calls, stream)
+    torch.cuda.synchronize()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    stream.synchronize()
+
+    clocks = ClockSampler(torch.cuda.current_device() if "CUDA_VISIBLE_DEVICES" not in os.environ
+                          else int(os.environ["CUDA_VISIBLE_DEVICES"].split(",")[dist.local]))
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    torch.cuda.synchronize()
+    dist.barrier()
+    clk = clocks.stop()
+    ms = ev0.elapsed_time(ev1)
+    ms_max = dist.max(ms)
+    if tern.tern_last_device_error(stream) != tern.TERN_OK:
+        raise SystemExit("device error during the timed region")
+
+    packed = wl.packed_bytes
+    alg = wl.algorithmic_bytes
+    step_ms = ms_max / args.steps
+    value = dist.world * packed * args.steps / (ms_max * 1e-3) / 1e9
+    us_per_call = 1e3 * step_ms / ncalls
+    per_launch_s = ms * 1e-3 / (args.steps * ncalls)
+    achieved = (alg / ncalls) / per_launch_s / 1e9
+    peak, peak_kind = peaks()
+    traffic, traffic_kernel = ncu_traffic(args.workload)
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, wl, stream, dist)
+
+    cpu = None
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        gbs, b, dt, desc = oracle_sample_rate(wl, max(1.0, 12.0 / threads), threads)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16 x, 2-bit ternary w, fp32 acc",
+        "data": "synthetic (seeded; code mix of the model page)",
+        "config": {"workload": f"{args.workload}: {wl.desc}", "calls_per_step": ncalls,
+                   "distinct_draws": wl.distinct, "packed_bytes_per_step": packed,
+                   "algorithmic_bytes_per_step": alg, "us_per_call": round(us_per_call, 4),
+                   "l2": "inputs larger than L2: each step streams %.0f MB of distinct buffers" % (packed / 1e6),
+                   "graph": "one CUDA graph per step, replayed", "parallelism": f"replicas x{dist.world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "traffic": traffic, "traffic_kernel": traffic_kernel,
+                     "bytes_per_launch": alg // ncalls},
+        "clocks": clk,
+        "gpu_launches": args.steps * ncalls,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_e2e(args, wl, stream, dist: Dist):
+    """Same metric through the public API with host buffers: each call copies
+    its activations from pinned host memory, runs, and copies its output back;
+    weights are the resident model."""
+    import torch
+
+    from packed_bit_gemv_tern_b300 import workloads
+
+    hx = [c.x.cpu().pin_memory() for c in wl.calls]
+    hy = [torch.empty(c.y.shape, dtype=torch.float32).pin_memory() for c in wl.calls]
+    h2d = sum(t.numel() * t.element_size() for t in hx)
+    d2h = sum(t.numel() * t.element_size() for t in hy)
+
+    def step():
+        for c, x, y in zip(wl.calls, hx, hy):
+            c.x.copy_(x, non_blocking=True)
+            workloads.run_call(c, stream)
+            y.copy_(c.y, non_blocking=True)
+        stream.synchronize()
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+        dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            step()
+        dt = time.perf_counter() - t0
+    dt = dist.max(dt)
+    return {"value": round(dist.world * wl.packed_bytes * args.e2e_steps / dt / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+            "how": "per call: pinned H2D of x, tern ABI call, D2H of y; no graph; host-timed"}
+
+
+def main():
+    args = parse()
+    dist = Dist()
+    try:
+        if args.impl == "reference":
+            return run_reference(args, dist)
+        return run_ours(args, dist)
+    finally:
+        dist.close()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

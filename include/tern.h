@@ -1,0 +1,160 @@
+/*
+ * tern.h -- C ABI of the B300 ternary packed-weight linear layer.
+ *
+ * The operation (Neutrino-1 8B model page, intro: "every one of its 252
+ * transformer linears is stored in a ternary-family weight format ... the
+ * weights stay bit-packed at rest and are decoded inside the matrix kernels";
+ * "Where the bytes live": per-row metadata of row dimensions, scales and row
+ * sums) is, for one projection with R output rows and K inputs,
+ *
+ *     y[m][r] = scale[r] * sum_{k < K} t[r][k] * x[m][k],   t[r][k] in {-1,0,+1}
+ *
+ * with the ternary matrix t kept in a 2-bit packed form and decoded inside the
+ * kernels (never expanded to a floating-point weight tensor in memory).
+ *
+ * Packed format.  The page calls its own format proprietary and never
+ * describes its bits, so this library fixes its own:
+ *   - K must be a multiple of 64 (pad rows with zero weights);
+ *   - codes: R * K/16 uint32 words, row-major and K-contiguous; row r owns
+ *     words [r*K/16, (r+1)*K/16) (16-byte aligned rows);
+ *   - column k of a row sits in word k/16 of that row at bits 2*(k%16) (b0,
+ *     low) and 2*(k%16)+1 (b1, high): least significant code first;
+ *   - (b1,b0): 00 -> 0, 01 -> +1, 11 -> -1 (2-bit two's complement);
+ *     10 is invalid: tern_pack never writes it, tern_validate reports it, and
+ *     the device kernels give an unspecified (but fault-free) result for it;
+ *   - scale: R fp32, applied after the sum;
+ *   - rowsum: R int32, rowsum[r] = sum_k t[r][k] (validation and closed-form
+ *     checks; the GEMV kernels do not read it).
+ *
+ * Activations x are bf16, passed as their uint16 bit patterns, row-major
+ * [M][K] (M = 1 for the GEMV).  Outputs are fp32, row-major [M][R].
+ *
+ * Conventions for every entry point:
+ *   - The caller owns every buffer; the library allocates no device memory
+ *     on any call and keeps no pointer after a call returns.
+ *   - Device entry points are asynchronous on the caller's stream
+ *     (a cudaStream_t passed as void*; NULL is the legacy default stream).
+ *     Arguments are checked on the host before anything is launched; a
+ *     failed check returns an error and launches nothing.
+ *   - No C++ exception crosses this boundary.
+ *   - A problem with rows == 0 is empty: it succeeds without a launch and its
+ *     pointers may be NULL.  K == 0 is valid and gives y = 0.
+ */
+#ifndef TERN_H
+#define TERN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TERN_ABI_VERSION 1
+
+/* Exported symbols (the library is built with hidden default visibility). */
+#if defined(__GNUC__)
+#define TERN_API __attribute__((visibility("default")))
+#else
+#define TERN_API
+#endif
+
+/* Largest activation block the device kernels stage on chip:
+ * m * k * 2 bytes (bf16) must not exceed this. */
+#define TERN_MAX_X_BYTES 196608
+/* Largest activation row count of tern_gemm_smallm*. */
+#define TERN_MAX_M 8
+
+typedef enum {
+    TERN_OK = 0,
+    TERN_ERR_NULL = 1,    /* a required pointer is NULL */
+    TERN_ERR_SHAPE = 2,   /* rows/k negative, k % 64 != 0, size limits, shape mismatch */
+    TERN_ERR_ALIGN = 3,   /* a pointer breaks its alignment rule */
+    TERN_ERR_BADCODE = 4, /* packed data holds the invalid pattern 10 */
+    TERN_ERR_ROWSUM = 5,  /* stored rowsum disagrees with the codes */
+    TERN_ERR_M_RANGE = 6, /* m outside [1, TERN_MAX_M] */
+    TERN_ERR_CUDA = 7,    /* a CUDA runtime call or launch failed */
+    TERN_ERR_TIMEOUT = 8, /* a device-side bounded wait ran out (see tern_last_device_error) */
+    TERN_ERR_VALUE = 9    /* an int8 weight given to tern_pack is not -1, 0 or +1 */
+} tern_status;
+
+/* One packed ternary matrix.  Pointers are device pointers for the device
+ * entry points.  codes: 16-byte aligned.  scale: 4-byte aligned.  rowsum:
+ * may be NULL (not read by the device kernels). */
+typedef struct {
+    int32_t rows;           /* R >= 0 */
+    int32_t k;              /* K >= 0, K % 64 == 0 */
+    const uint32_t *codes;  /* R * K/16 words */
+    const float *scale;     /* R */
+    const int32_t *rowsum;  /* R, or NULL */
+} tern_matrix;
+
+/* ---------------------------------------------------------------------- */
+/* Host-side packer and validator (host memory, synchronous).              */
+/* ---------------------------------------------------------------------- */
+
+/* Pack an int8 matrix t [rows][k] (values -1, 0, +1) into codes
+ * [rows][k/16] and write rowsum[rows] (rowsum may be NULL).
+ * The per-row metadata follows "Where the bytes live" (scales and row sums).
+ * Errors: TERN_ERR_NULL, TERN_ERR_SHAPE (k % 64, negative sizes),
+ * TERN_ERR_VALUE (a weight outside {-1,0,+1}; codes are then incomplete). */
+TERN_API tern_status tern_pack(const int8_t *t, int32_t rows, int32_t k,
+                      uint32_t *codes, int32_t *rowsum);
+
+/* Check packed codes: no invalid pattern, and (if rowsum != NULL) every
+ * stored rowsum equals the sum of its row.  counts_out (may be NULL) receives
+ * {zeros, plus ones, minus ones} over the whole matrix: the statistics the
+ * model page reports in "Inside the coded lane".
+ * Errors: TERN_ERR_NULL, TERN_ERR_SHAPE, TERN_ERR_BADCODE (first bad word
+ * stops the scan; counts are then partial), TERN_ERR_ROWSUM. */
+TERN_API tern_status tern_validate(const uint32_t *codes, int32_t rows, int32_t k,
+                          const int32_t *rowsum, int64_t counts_out[3]);
+
+/* ---------------------------------------------------------------------- */
+/* Device entry points (device pointers, asynchronous on `stream`).        */
+/* ---------------------------------------------------------------------- */
+
+/* Decode a packed matrix to int8 t_out [rows][k] (debug / exactness gate;
+ * "decoded inside the matrix kernels" made visible).  t_out: 16-byte aligned.
+ * The invalid pattern decodes to -2. */
+TERN_API tern_status tern_unpack(const tern_matrix *w, int8_t *t_out, void *stream);
+
+/* M = 1 decode-time GEMV: y[r] = scale[r] * sum_k t[r][k] x[k].
+ * x: k bf16 values, 16-byte aligned.  y: rows fp32, 4-byte aligned.
+ * x and y must not overlap the matrix.  Limit: 2*k <= TERN_MAX_X_BYTES. */
+TERN_API tern_status tern_gemv(const tern_matrix *w, const uint16_t *x, float *y, void *stream);
+
+/* Fused gated feed-forward pair (spec table: gated SwiGLU feed-forward,
+ * three linears per layer): h[r] = silu(g[r]) * u[r] with
+ * g = gate projection of x, u = up projection of x, silu(z) = z/(1+exp(-z)).
+ * gate and up must have equal rows and k.  h: rows fp32. */
+TERN_API tern_status tern_gemv_swiglu(const tern_matrix *gate, const tern_matrix *up,
+                             const uint16_t *x, float *h, void *stream);
+
+/* Small-M GEMM for speculative verification (the page's verifier scores a
+ * six-token draft plus one token in one forward pass, so M = 7):
+ * y[i][r] = scale[r] * sum_k t[r][k] x[i][k] for i < m, 1 <= m <= TERN_MAX_M.
+ * x: [m][k] bf16, 16-byte aligned.  y: [m][rows] fp32.
+ * Errors add TERN_ERR_M_RANGE.  Limit: m*k*2 <= TERN_MAX_X_BYTES. */
+TERN_API tern_status tern_gemm_smallm(const tern_matrix *w, const uint16_t *x, int32_t m,
+                             float *y, void *stream);
+
+/* Small-M fused gate/up: h[i][r] = silu(g[i][r]) * u[i][r], i < m. */
+TERN_API tern_status tern_gemm_smallm_swiglu(const tern_matrix *gate, const tern_matrix *up,
+                                    const uint16_t *x, int32_t m, float *h, void *stream);
+
+/* Synchronise `stream`, then report and clear the device error word that
+ * bounded device-side waits set when they run out (TERN_ERR_TIMEOUT), or a
+ * pending CUDA error (TERN_ERR_CUDA).  TERN_OK otherwise. */
+TERN_API tern_status tern_last_device_error(void *stream);
+
+/* Static description of a status code (never NULL). */
+TERN_API const char *tern_status_str(tern_status s);
+
+/* TERN_ABI_VERSION of the loaded library. */
+TERN_API int32_t tern_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TERN_H */

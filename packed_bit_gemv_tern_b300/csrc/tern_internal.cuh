@@ -1,0 +1,30 @@
+// tern_internal.cuh -- declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "tern.h"
+
+namespace tern {
+
+constexpr int kCcThreads = 256;  // CUDA-core kernels: 8 warps per CTA
+
+int sm_count();
+tern_status check_matrix(const tern_matrix *w);
+
+// CUDA-core kernels (tern_cuda.cu); u == nullptr means a plain projection.
+tern_status gemm_cc(const tern_matrix *g, const tern_matrix *u, const uint16_t *x, int m, float *y,
+                    cudaStream_t s);
+
+// Kernel choice per entry point (tern_dispatch.cu).
+tern_status gemv_dispatch(const tern_matrix *w, const uint16_t *x, float *y, cudaStream_t s);
+tern_status swiglu_dispatch(const tern_matrix *g, const tern_matrix *u, const uint16_t *x, int m,
+                            float *h, cudaStream_t s);
+tern_status smallm_dispatch(const tern_matrix *w, const uint16_t *x, int m, float *y, cudaStream_t s);
+
+// Reads and clears every device error word (TERN_OK when all are clear).
+tern_status take_device_error();
+
+}  // namespace tern

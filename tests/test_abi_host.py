@@ -1,0 +1,136 @@
+"""Host-side tests of the C ABI (no GPU needed): the library loads, exports
+every symbol include/tern.h declares, packs and validates exactly like the
+oracle's independent encoder, and rejects bad arguments before launching
+anything."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import packed_bit_gemv_tern_b300 as tern
+from packed_bit_gemv_tern_b300 import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn)).read()
+            names += re.findall(r"^TERN_API[^(]*?\b(tern_\w+)\s*\(", src, flags=re.M)
+    return names
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from packed_bit_gemv_tern_b300 import build
+    build.build()
+    return tern.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(tern.ABI_FUNCTIONS) <= set(names)
+    assert tern.tern_abi_version() == 1
+
+
+def test_status_strings(lib):
+    for s in range(10):
+        assert tern.tern_status_str(s)
+    assert "unknown" in tern.tern_status_str(99)
+
+
+@pytest.mark.parametrize("rows,k,seed", [(1, 64, 0), (7, 128, 1), (33, 4096, 2), (5, 12288, 3), (0, 64, 4), (3, 0, 5)])
+def test_pack_matches_oracle_encoder(lib, rows, k, seed):
+    rng = np.random.default_rng(seed)
+    t = synth.ternary(rng, rows, k)
+    codes, rowsum = tern.tern_pack(t)
+    if rows and k:
+        assert np.array_equal(codes, oracle.pack(t))
+    orc_rowsum, orc_counts = oracle.stats(codes, k) if rows else (np.zeros(0), np.zeros(3))
+    assert np.array_equal(rowsum, orc_rowsum.astype(np.int32))
+    counts = tern.tern_validate(codes, k, rowsum)
+    assert counts.tolist() == [int((t == 0).sum()), int((t == 1).sum()), int((t == -1).sum())]
+    if rows:
+        assert counts.tolist() == orc_counts.tolist()
+
+
+def test_pack_rejects(lib):
+    with pytest.raises(tern.TernError) as e:
+        tern.tern_pack(np.zeros((2, 48), np.int8))
+    assert e.value.status == tern.TERN_ERR_SHAPE
+    bad = np.zeros((2, 64), np.int8)
+    bad[1, 5] = -2
+    with pytest.raises(tern.TernError) as e:
+        tern.tern_pack(bad)
+    assert e.value.status == tern.TERN_ERR_VALUE
+
+
+def test_validate_rejects(lib):
+    rng = np.random.default_rng(9)
+    t = synth.ternary(rng, 4, 128)
+    codes, rowsum = tern.tern_pack(t)
+    bad = codes.copy()
+    bad[2, 3] |= np.uint32(0x2 << 10)
+    bad[2, 3] &= ~np.uint32(0x1 << 10)
+    with pytest.raises(tern.TernError) as e:
+        tern.tern_validate(bad, 128)
+    assert e.value.status == tern.TERN_ERR_BADCODE
+    rs = rowsum.copy()
+    rs[1] += 1
+    with pytest.raises(tern.TernError) as e:
+        tern.tern_validate(codes, 128, rs)
+    assert e.value.status == tern.TERN_ERR_ROWSUM
+
+
+def _mat(rows, k, codes=0x1000, scale=0x2000):
+    return tern.CMatrix(rows, k, codes, scale, None)
+
+
+def _call(lib, name, *args):
+    return getattr(lib, name)(*args)
+
+
+def test_device_entry_points_reject_before_launch(lib):
+    """Every case fails a host check, so nothing reaches the GPU (or the
+    missing GPU).  Pointers are fake but never dereferenced."""
+    ok_m = _mat(4, 64)
+    x, y = ctypes.c_void_p(0x3000), ctypes.c_void_p(0x4000)
+    ref = ctypes.byref
+    assert lib.tern_gemv(None, x, y, None) == tern.TERN_ERR_NULL
+    assert lib.tern_gemv(ref(_mat(4, 48)), x, y, None) == tern.TERN_ERR_SHAPE
+    assert lib.tern_gemv(ref(_mat(-1, 64)), x, y, None) == tern.TERN_ERR_SHAPE
+    assert lib.tern_gemv(ref(_mat(4, 64, codes=0x1004)), x, y, None) == tern.TERN_ERR_ALIGN
+    assert lib.tern_gemv(ref(_mat(4, 64, scale=0x2002)), x, y, None) == tern.TERN_ERR_ALIGN
+    assert lib.tern_gemv(ref(_mat(4, 64, codes=0)), x, y, None) == tern.TERN_ERR_NULL
+    assert lib.tern_gemv(ref(ok_m), None, y, None) == tern.TERN_ERR_NULL
+    assert lib.tern_gemv(ref(ok_m), x, None, None) == tern.TERN_ERR_NULL
+    assert lib.tern_gemv(ref(ok_m), ctypes.c_void_p(0x3008), y, None) == tern.TERN_ERR_ALIGN
+    assert lib.tern_gemv(ref(ok_m), x, ctypes.c_void_p(0x4002), None) == tern.TERN_ERR_ALIGN
+    big = _mat(4, 98368)  # 2*k > TERN_MAX_X_BYTES
+    assert lib.tern_gemv(ref(big), x, y, None) == tern.TERN_ERR_SHAPE
+    # small-M range and limits
+    for m in (0, 9, -1):
+        assert lib.tern_gemm_smallm(ref(ok_m), x, m, y, None) == tern.TERN_ERR_M_RANGE
+    assert lib.tern_gemm_smallm(ref(_mat(4, 12352)), x, 8, y, None) == tern.TERN_ERR_SHAPE
+    # SwiGLU pair mismatch / missing up
+    assert lib.tern_gemv_swiglu(ref(ok_m), None, x, y, None) == tern.TERN_ERR_NULL
+    assert lib.tern_gemv_swiglu(ref(ok_m), ref(_mat(5, 64)), x, y, None) == tern.TERN_ERR_SHAPE
+    assert lib.tern_gemv_swiglu(ref(ok_m), ref(_mat(4, 128)), x, y, None) == tern.TERN_ERR_SHAPE
+    assert lib.tern_gemm_smallm_swiglu(ref(ok_m), ref(ok_m), x, 9, y, None) == tern.TERN_ERR_M_RANGE
+    # unpack
+    assert lib.tern_unpack(ref(ok_m), None, None) == tern.TERN_ERR_NULL
+    assert lib.tern_unpack(ref(ok_m), ctypes.c_void_p(0x5001), None) == tern.TERN_ERR_ALIGN
+    # empty problems succeed without a launch, with NULL pointers
+    empty = tern.CMatrix(0, 64, None, None, None)
+    assert lib.tern_gemv(ref(empty), None, None, None) == tern.TERN_OK
+    assert lib.tern_gemm_smallm(ref(empty), None, 3, None, None) == tern.TERN_OK
+    assert lib.tern_gemv_swiglu(ref(empty), ref(empty), None, None, None) == tern.TERN_OK
+    assert lib.tern_unpack(ref(empty), None, None) == tern.TERN_OK
