@@ -1,24 +1,50 @@
 // tern_dispatch.cu -- which kernel serves which entry point.
+//
+// The tensor-core kernel (tern_mma.cu) serves every entry point.  K == 0 (an
+// empty sum, y = 0) goes to the CUDA-core kernel, which needs no weight
+// stream.  Setting TERN_KERNEL=cuda_core in the environment before the first
+// call routes everything to the CUDA-core kernels (tern_cuda.cu) instead; it
+// exists to compare the two designs on the same workloads.
+#include <cstdlib>
+#include <cstring>
+
 #include "tern_internal.cuh"
 
 namespace tern {
 
+static bool use_cuda_core()
+{
+    static int v = -1;
+    if (v < 0) {
+        const char *e = std::getenv("TERN_KERNEL");
+        v = (e != nullptr && std::strcmp(e, "cuda_core") == 0) ? 1 : 0;
+    }
+    return v == 1;
+}
+
+static tern_status run(const tern_matrix *g, const tern_matrix *u, const uint16_t *x, int m, float *y,
+                       cudaStream_t s)
+{
+    if (g->k == 0 || use_cuda_core()) return gemm_cc(g, u, x, m, y, s);
+    return gemm_mma(g, u, x, m, y, s);
+}
+
 tern_status gemv_dispatch(const tern_matrix *w, const uint16_t *x, float *y, cudaStream_t s)
 {
-    return gemm_cc(w, nullptr, x, 1, y, s);
+    return run(w, nullptr, x, 1, y, s);
 }
 
 tern_status swiglu_dispatch(const tern_matrix *g, const tern_matrix *u, const uint16_t *x, int m,
                             float *h, cudaStream_t s)
 {
-    return gemm_cc(g, u, x, m, h, s);
+    return run(g, u, x, m, h, s);
 }
 
 tern_status smallm_dispatch(const tern_matrix *w, const uint16_t *x, int m, float *y, cudaStream_t s)
 {
-    return gemm_cc(w, nullptr, x, m, y, s);
+    return run(w, nullptr, x, m, y, s);
 }
 
-tern_status take_device_error() { return TERN_OK; }
+tern_status take_device_error() { return take_mma_error(); }
 
 }  // namespace tern

@@ -18,6 +18,11 @@ tern_status check_matrix(const tern_matrix *w);
 tern_status gemm_cc(const tern_matrix *g, const tern_matrix *u, const uint16_t *x, int m, float *y,
                     cudaStream_t s);
 
+// Tensor-core kernels (tern_mma.cu); same contract as gemm_cc.
+tern_status gemm_mma(const tern_matrix *g, const tern_matrix *u, const uint16_t *x, int m, float *y,
+                     cudaStream_t s);
+tern_status take_mma_error();
+
 // Kernel choice per entry point (tern_dispatch.cu).
 tern_status gemv_dispatch(const tern_matrix *w, const uint16_t *x, float *y, cudaStream_t s);
 tern_status swiglu_dispatch(const tern_matrix *g, const tern_matrix *u, const uint16_t *x, int m,

@@ -1,0 +1,671 @@
+// tern_mma.cu -- tensor-core ternary GEMV / small-M GEMM for sm_103a.
+//
+// What is computed (Neutrino-1 8B model page, intro: the ternary weights stay
+// bit-packed and are decoded inside the matrix kernels; spec table: gated
+// SwiGLU feed-forward; "Where the bytes live": per-row scales):
+//     y[m][r] = scale[r] * sum_k t[r][k] x[m][k]      m < M (M <= 8)
+//     h[m][r] = silu(y_gate[m][r]) * y_up[m][r]       (SwiGLU pair)
+//
+// Layout of the work: one CTA per SM owns 128 weight rows (the MMA's M) and
+// one K range; a cluster of S CTAs splits K and reduces through distributed
+// shared memory.  Roles (13 warps):
+//   * warp 0, lane 0: TMA producer.  2-D tiled bulk copies bring 128 rows x
+//     512 codes (16 KB, 128-byte swizzle) per stage into a shared-memory ring.
+//     Weights do not depend on the previous kernel, so the first stages are
+//     requested before anything waits on it (programmatic dependent launch).
+//   * warps 1-4: B operand staging.  After griddepcontrol.wait they turn the
+//     activations of the K range into the MMA's B operand.  Each bf16 value x
+//     of activation row m is split into two e4m3 terms under a per-row
+//     power-of-two scale 2^s (the row's largest |x| lands in [128, 256)):
+//     x*2^s = hi + lo/16, hi = RN_e4m3(x*2^s), lo = RN_e4m3((x*2^s - hi)*16).
+//     A bf16 value has 8 significant bits and each e4m3 term holds 4, so with
+//     2^e <= max|x| < 2^(e+1) the split is exact for every |x| >= 2^(e-13);
+//     smaller elements carry an absolute error of at most 2^(e-21).  Column 2m
+//     of B holds hi, 2m+1 lo (N = 16 covers M <= 8).
+//   * warps 5-12: two decoder warpgroups taking alternate chunks of 8 words
+//     (128 codes) per row.  Thread i owns weight row i (TMEM lane i).  Each
+//     32-bit word (16 codes) becomes four registers of four e4m3 bytes:
+//         R_j = (w << (6 - 2j)) & 0xC0C0C0C0,   byte b of R_j <- code 4b + j
+//     which puts b1 on the sign bit and b0 on the exponent's top bit: exactly
+//     0, +2 or -2 in e4m3 (the invalid code 10 gives -0).  No multiply touches
+//     a weight.  The 32 registers go to the chunk's TMEM slot (tcgen05.st);
+//     the group's four warps meet at a named barrier, then warp q issues the
+//     chunk's K=32 step q (tcgen05.mma kind::f8f6f4, A e4m3 from TMEM, B e4m3
+//     from shared memory, M = 128, N = 16) into its own fp32 accumulator
+//     D[g][q] and commits the slot back.  Spreading the issue over eight warps
+//     keeps the per-thread issue cost (about 45 cycles per MMA) off the
+//     critical path.
+//   * epilogue: the eight accumulators are summed (tcgen05.ld), hi/lo columns
+//     rescaled by 2^-s and 2^-(s+4), split-K partials pushed into rank 0's
+//     shared memory and summed there in rank order after one cluster barrier,
+//     then y = scale * (0.5 * sum) (the weights entered as +-2), or
+//     silu(gate) * up for the SwiGLU pair (tile rows 0-63 are gate rows,
+//     64-127 the matching up rows).
+// Every mbarrier wait is bounded; on time-out the kernel records the error,
+// stops, waits for its own copies and MMAs, releases its tensor memory and
+// returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+
+#include "tern.h"
+#include "tern_internal.cuh"
+#include "tern_ptx.cuh"
+
+namespace tern {
+
+namespace {
+
+constexpr int kThreads = 416;             // 13 warps
+constexpr int kStagerWarps = 4;           // warps 1-4: B operand staging, then MMA issue
+constexpr int kStagers = 32 * kStagerWarps;
+constexpr int kIssuers = kStagerWarps;    // one MMA issuer (lane 0) per staging warp
+constexpr int kFirstDecWarp = 1 + kStagerWarps;  // warps 5-12: decoders (two warpgroups)
+constexpr int kStageWords = 32;           // words per row per stage (512 codes, 128 B)
+constexpr int kStageBytes = 128 * 128;    // 128 rows x 128 B
+constexpr int kChunkWords = 8;            // words per row per decode chunk (2 x 16 B)
+constexpr int kBBytesPerWord = 256;       // B operand: 16 rows x 16 e4m3 per word
+constexpr int kASlots = 3;                // TMEM A slots, one stage (128 columns) each
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kDCol = kASlots * 128;  // accumulators D[k], k < kIssuers, at [kDCol, kDCol + 16 kIssuers)
+constexpr int kMaxWStages = 8;
+constexpr int kSmemLimit = 227 * 1024;
+// Every CTA allocates all 512 TMEM columns.  Asking for more than half of the
+// SM's shared memory keeps one CTA per SM, so tcgen05.alloc never waits for a
+// CTA of the same launch (which could itself be waiting, at a cluster barrier,
+// on the one that waits).
+constexpr uint32_t kMinSmem = 118 * 1024;
+
+// Instruction descriptor: kind::f8f6f4, D fp32, A e4m3, B e4m3, K-major A and
+// B, N = 16, M = 128.
+constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
+
+__device__ unsigned int g_mma_error;  // bit 0: a bounded wait ran out
+
+struct MmaParams {
+    const float *scale_g;
+    const float *scale_u;
+    const uint16_t *x;
+    float *y;
+    int rows;
+    int k;
+    int m;            // activation rows (1..8)
+    int total_st;     // stages over the whole K
+    int per_st;       // stages per cluster rank
+    int split;        // cluster size
+    int n_wst;        // shared-memory weight ring depth
+    uint32_t off_b;   // shared-memory byte offsets from the 1024-aligned base
+    uint32_t off_red;
+    uint32_t off_xch;
+    uint32_t off_bar;
+};
+
+// Barrier block layout (byte offsets from off_bar).
+constexpr uint32_t kBarWFull = 0;
+constexpr uint32_t kBarWEmpty = kBarWFull + 8 * kMaxWStages;
+constexpr uint32_t kBarAFull = kBarWEmpty + 8 * kMaxWStages;       // [kASlots]
+constexpr uint32_t kBarAEmpty = kBarAFull + 8 * kASlots;            // [kASlots]
+constexpr uint32_t kBarBReady = kBarAEmpty + 8 * kASlots;
+constexpr uint32_t kBarDFull = kBarBReady + 8;                      // one arrival per issuer
+constexpr uint32_t kWords = kBarDFull + 8;                          // uint32 scratch after barriers
+// words: [0] tmem base, [1] abort, [2] bit mask of written accumulators, [4..11] max|x| bits per row
+constexpr uint32_t kBarBytes = kWords + 16 * 4;
+
+// Shared-memory descriptor of a K-major, unswizzled operand made of 8-row x
+// 16-byte core matrices: adjacent core matrices along K are 256 B apart (LBO),
+// along N 128 B apart (SBO).
+__device__ __forceinline__ uint64_t b_desc(uint32_t addr)
+{
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)(256u >> 4) << 16) | ((uint64_t)(128u >> 4) << 32) |
+           (1ull << 46);
+}
+
+struct Waiter {
+    volatile uint32_t *abort_flag;  // shared
+    __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity)
+    {
+        if (*abort_flag) return false;
+        const long long t0 = clock64();
+        uint32_t spins = 0;
+        while (!ptx::mbar_try_wait(bar, parity)) {
+            if ((++spins & 15u) == 0u) {
+                if (*abort_flag) return false;
+                if (clock64() - t0 > (1ll << 31)) {  // ~1 s at 2 GHz
+                    atomicOr(&g_mma_error, 1u);
+                    *abort_flag = 1u;
+                    return false;
+                }
+            }
+        }
+        return true;
+    }
+};
+
+// Bounded wait that ignores the abort flag (used to drain in-flight work).
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
+{
+    const long long t0 = clock64();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > (1ll << 31)) {
+            atomicOr(&g_mma_error, 1u);
+            return;
+        }
+    }
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+// 2^e as an fp32 (e in [-126, 127]).
+__device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
+
+// Splits a pair of bf16 activations (one 32-bit word, low half = even k)
+// scaled by sc = 2^s into e4m3 bytes with x*2^s = hi + lo/16: hi is x*2^s
+// rounded to nearest e4m3, lo = (x*2^s - hi)*16 rounded to nearest e4m3 (the
+// difference is formed exactly in f16).  For x*2^s >= 2^-6 hi keeps 4
+// significant bits and lo the remaining <= 4, so the pair is exact whenever lo
+// is an e4m3 normal or zero; below that both round to e4m3 subnormals (steps
+// of 2^-9), bounding the error by 2^-14 in units of x*2^s.
+// Output: hp/lp = two bytes each, low byte for the even k.
+__device__ __forceinline__ void split_pair(uint32_t v, float sc, uint32_t &hp, uint32_t &lp)
+{
+    const float xa = __uint_as_float(v << 16) * sc;
+    const float xb = __uint_as_float(v & 0xFFFF0000u) * sc;
+    uint16_t h, l;
+    uint32_t xh, hh, d;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(xb), "f"(xa));
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hh) : "h"(h));
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(xh) : "f"(xb), "f"(xa));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(xh), "r"(hh));
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(d), "r"(0x4C004C00u));  // x16
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l) : "r"(d));
+    hp = h;
+    lp = l;
+}
+
+template <bool SWIGLU>
+__global__ void __launch_bounds__(kThreads, 1)
+k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_u, const MmaParams p)
+{
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char *gbase = smem_raw + (base - raw);
+
+    const uint32_t wbuf = base;
+    const uint32_t bbuf = base + p.off_b;
+    float *red = reinterpret_cast<float *>(gbase + p.off_red);   // [split][128][8]
+    float *xch = reinterpret_cast<float *>(gbase + p.off_xch);   // [64][8]
+    const uint32_t bars = base + p.off_bar;
+    uint32_t *words = reinterpret_cast<uint32_t *>(gbase + p.off_bar + kWords);
+    volatile uint32_t *abort_flag = words + 1;
+    uint32_t *xmax = words + 4;  // [8] max |x| (fp32 bits) per activation row
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5, lane = tid & 31;
+    const int split = p.split;
+    const int rank = (int)(blockIdx.x % (unsigned)split);
+    const int tile = (int)(blockIdx.x / (unsigned)split);
+    const int st0 = rank * p.per_st;
+    const int st1 = min(p.total_st, st0 + p.per_st);
+    const int n_st = max(0, st1 - st0);
+    const int n_chunks = n_st * (kStageWords / kChunkWords);  // 4 chunks per stage
+    const int n_wst = p.n_wst;
+    const int row0 = SWIGLU ? tile * 64 : tile * 128;
+    const int m = p.m;
+
+    auto issue = [&](int s) {
+        const int slot = s % n_wst;
+        const uint32_t dst = wbuf + slot * kStageBytes;
+        const uint32_t full = bars + kBarWFull + 8 * slot;
+        const int c0 = (st0 + s) * kStageWords;
+        ptx::mbar_arrive_expect_tx(full, kStageBytes);
+        if constexpr (SWIGLU) {
+            ptx::tma_load_2d(dst, &tm_g, c0, row0, full);
+            ptx::tma_load_2d(dst + kStageBytes / 2, &tm_u, c0, row0, full);
+        } else {
+            ptx::tma_load_2d(dst, &tm_g, c0, row0, full);
+        }
+    };
+
+    // ---- prologue: barriers, first weight copies, tensor memory
+    int issued = 0;
+    if (tid == 0) {
+        for (int s = 0; s < n_wst; ++s) {
+            ptx::mbar_init(bars + kBarWFull + 8 * s, 1);
+            ptx::mbar_init(bars + kBarWEmpty + 8 * s, 4);  // the four warps of the group that read it
+        }
+        for (int s = 0; s < kASlots; ++s) {
+            ptx::mbar_init(bars + kBarAFull + 8 * s, 4);   // the four warps that wrote it
+            ptx::mbar_init(bars + kBarAEmpty + 8 * s, kIssuers);
+        }
+        ptx::mbar_init(bars + kBarBReady, kStagers);
+        ptx::mbar_init(bars + kBarDFull, kIssuers);
+        for (int j = 1; j < 16; ++j) words[j] = 0u;
+        ptx::fence_proxy_async_smem();
+        if (n_st > 0) {
+            ptx::prefetch_tmap(&tm_g);
+            if (SWIGLU) ptx::prefetch_tmap(&tm_u);
+            for (; issued < n_st && issued < n_wst; ++issued) issue(issued);
+        }
+    }
+    if (warp == 0) {
+        __syncwarp();
+        ptx::tmem_alloc(ptx::smem_u32(words), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = words[0];
+    if (tid == 0) ptx::grid_dep_launch();
+    Waiter waiter{abort_flag};
+
+    if (warp == 0) {
+        // ----------------------------------------------------------- producer
+        if (lane == 0) {
+            for (; issued < n_st; ++issued) {
+                const int slot = issued % n_wst;
+                if (!waiter.wait(bars + kBarWEmpty + 8 * slot, ((issued / n_wst) - 1) & 1)) break;
+                issue(issued);
+            }
+            // every issued copy must land before the CTA may exit
+            for (int s = (issued > n_wst ? issued - n_wst : 0); s < issued; ++s)
+                drain_wait(bars + kBarWFull + 8 * (s % n_wst), (s / n_wst) & 1);
+        }
+    } else if (warp <= kStagerWarps) {
+        // ------------------------------------------------- B operand staging
+        // Only these warps read data the previous grid may have written (the
+        // activations), so only they wait for it; every MMA waits for b_ready.
+        ptx::grid_dep_wait();
+        const int st_tid = tid - 32;
+        const int n_words = n_st * kStageWords;
+        const int k0 = st0 * kStageWords * 16;
+        const int n_items = m * n_words;  // (activation row, word) pairs with data
+        // Items are processed in batches of kStageItems per thread: all loads of
+        // a batch are issued before any is used, so a batch costs one memory
+        // latency.  Small problems (n_items <= kStagers * kStageItems) keep
+        // their activations in registers between the max pass and the split.
+        constexpr int kStageItems = 4;
+        uint4 xa[kStageItems], xb[kStageItems];
+        const bool resident = n_items <= kStagers * kStageItems;
+        auto load_batch = [&](int first) {
+#pragma unroll
+            for (int t = 0; t < kStageItems; ++t) {
+                const int item = first + t * kStagers;
+                xa[t] = make_uint4(0, 0, 0, 0);
+                xb[t] = make_uint4(0, 0, 0, 0);
+                if (item < n_items) {
+                    const int mm = item / n_words, wi = item - mm * n_words;
+                    const int kk = k0 + 16 * wi;
+                    if (kk < p.k) {
+                        const uint4 *src = reinterpret_cast<const uint4 *>(p.x + (size_t)mm * p.k + kk);
+                        xa[t] = src[0];
+                        xb[t] = src[1];
+                    }
+                }
+            }
+        };
+        for (int first = st_tid; first < n_items; first += kStagers * kStageItems) {  // max |x| per row
+            load_batch(first);
+#pragma unroll
+            for (int t = 0; t < kStageItems; ++t) {
+                const int item = first + t * kStagers;
+                if (item < n_items) {
+                    const uint32_t v[8] = {xa[t].x, xa[t].y, xa[t].z, xa[t].w, xb[t].x, xb[t].y, xb[t].z, xb[t].w};
+                    uint32_t mx = 0;
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) mx = max(mx, max((v[q] << 16) & 0x7FFF0000u, v[q] & 0x7FFF0000u));
+                    atomicMax(&xmax[item / n_words], mx);
+                }
+            }
+        }
+        ptx::named_bar_sync(3, kStagers);
+        for (int first = st_tid; first < n_items; first += kStagers * kStageItems) {  // e4m3 pieces
+            if (!resident) load_batch(first);
+#pragma unroll
+            for (int t = 0; t < kStageItems; ++t) {
+                const int item = first + t * kStagers;
+                if (item >= n_items) break;
+                const int mm = item / n_words, wi = item - mm * n_words;
+                uint4 hi4 = make_uint4(0, 0, 0, 0), lo4 = make_uint4(0, 0, 0, 0);
+                if (k0 + 16 * wi < p.k) {
+                    const uint32_t mb = xmax[mm];
+                    const int e = mb == 0 ? 0 : (int)(mb >> 23) - 127;
+                    const float sc = exp2i(min(max(7 - e, -120), 120));
+                    const uint32_t v[8] = {xa[t].x, xa[t].y, xa[t].z, xa[t].w, xb[t].x, xb[t].y, xb[t].z, xb[t].w};
+                    uint32_t hp[8], lp[8];  // per k pair: two e4m3 bytes (low byte = even k)
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) split_pair(v[q], sc, hp[q], lp[q]);
+                    // byte b of output word j holds k offset 4b + j (a 4x4 transpose)
+                    const uint32_t h02 = hp[0] | (hp[2] << 16), h46 = hp[4] | (hp[6] << 16);
+                    const uint32_t h13 = hp[1] | (hp[3] << 16), h57 = hp[5] | (hp[7] << 16);
+                    const uint32_t l02 = lp[0] | (lp[2] << 16), l46 = lp[4] | (lp[6] << 16);
+                    const uint32_t l13 = lp[1] | (lp[3] << 16), l57 = lp[5] | (lp[7] << 16);
+                    hi4 = make_uint4(__byte_perm(h02, h46, 0x6420), __byte_perm(h02, h46, 0x7531),
+                                     __byte_perm(h13, h57, 0x6420), __byte_perm(h13, h57, 0x7531));
+                    lo4 = make_uint4(__byte_perm(l02, l46, 0x6420), __byte_perm(l02, l46, 0x7531),
+                                     __byte_perm(l13, l57, 0x6420), __byte_perm(l13, l57, 0x7531));
+                }
+                const int nh = 2 * mm, nl = 2 * mm + 1;  // B rows of the two pieces
+                const uint32_t at = bbuf + (uint32_t)wi * kBBytesPerWord;
+                ptx::sts128(at + (uint32_t)((nh >> 3) * 128 + (nh & 7) * 16), hi4);
+                ptx::sts128(at + (uint32_t)((nl >> 3) * 128 + (nl & 7) * 16), lo4);
+            }
+        }
+        // rows n >= 2m of B are zero
+        for (int item = st_tid; item < (8 - m) * n_words; item += kStagers) {
+            const int mm = m + item / n_words, wi = item % n_words;
+            const uint32_t at = bbuf + (uint32_t)wi * kBBytesPerWord;
+            const int nh = 2 * mm, nl = 2 * mm + 1;
+            ptx::sts128(at + (uint32_t)((nh >> 3) * 128 + (nh & 7) * 16), make_uint4(0, 0, 0, 0));
+            ptx::sts128(at + (uint32_t)((nl >> 3) * 128 + (nl & 7) * 16), make_uint4(0, 0, 0, 0));
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::mbar_arrive(bars + kBarBReady);
+        // ------------------------------------------------------- MMA issue
+        // Issuer k takes the K=32 steps 4k..4k+3 of every stage (16 steps of
+        // two words each) into its own accumulator D[k].
+        const int k_iss = warp - 1;
+        if (lane == 0) {
+            bool ok = waiter.wait(bars + kBarBReady, 0);  // all staging warps are done
+            const uint32_t d = tmem + kDCol + 16u * (uint32_t)k_iss;
+            for (int st = 0; st < n_st && ok; ++st) {
+                const int slot = st % kASlots;
+                if (!waiter.wait(bars + kBarAFull + 8 * slot, (st / kASlots) & 1)) break;
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const int step = 4 * k_iss + t;               // K=32 step within the stage
+                    const int wi = st * kStageWords + 2 * step;   // its first word
+                    ptx::mma_ts_f8f6f4(d, tmem + (uint32_t)(slot * 128 + step * 8),
+                                       b_desc(bbuf + (uint32_t)wi * kBBytesPerWord), kIdesc,
+                                       (st | t) != 0 ? 1u : 0u);
+                }
+                ptx::mma_commit(bars + kBarAEmpty + 8 * slot);
+                if (st == 0) atomicOr(&words[2], 1u << k_iss);  // accumulator written
+            }
+            ptx::mma_commit(bars + kBarDFull);  // arrives when this issuer's MMAs are done
+        }
+    } else {
+        // ----------------------------------------------------------- decoders
+        // Warpgroup g decodes every other stage; thread i owns row i (TMEM lane
+        // i).  A stage is 32 words per row: four chunks of 8 words, each
+        // stored to 32 columns of the stage's TMEM slot.  Only lane 0 polls
+        // barriers; the warp follows it.
+        const int g = (warp - kFirstDecWarp) >> 2;
+        const int quad = warp & 3;                  // TMEM lane quadrant this warp may touch
+        const int i = quad * 32 + lane;             // weight row within the tile == TMEM lane
+        const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+        const uint32_t row_addr = wbuf + (uint32_t)i * 128u;
+        for (int st = g; st < n_st; st += 2) {
+            const int wslot = st % n_wst;
+            const int aslot = st % kASlots;
+            uint32_t ok = 1u;
+            if (lane == 0) {
+                ok = waiter.wait(bars + kBarWFull + 8 * wslot, (st / n_wst) & 1) ? 1u : 0u;
+                if (ok && st >= kASlots) ok = waiter.wait(bars + kBarAEmpty + 8 * aslot, ((st / kASlots) - 1) & 1) ? 1u : 0u;
+            }
+            if (__shfl_sync(0xFFFFFFFFu, ok, 0) == 0u) break;
+            ptx::tc_fence_after();
+            const uint32_t srow = row_addr + (uint32_t)wslot * kStageBytes;
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                const uint4 v0 = ptx::lds128(srow + ((uint32_t)((2 * c) ^ (i & 7)) << 4));
+                const uint4 v1 = ptx::lds128(srow + ((uint32_t)((2 * c + 1) ^ (i & 7)) << 4));
+                const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+                uint32_t r[32];
+#pragma unroll
+                for (int w8 = 0; w8 < 8; ++w8) {
+                    r[4 * w8 + 0] = (wv[w8] << 6) & 0xC0C0C0C0u;
+                    r[4 * w8 + 1] = (wv[w8] << 4) & 0xC0C0C0C0u;
+                    r[4 * w8 + 2] = (wv[w8] << 2) & 0xC0C0C0C0u;
+                    r[4 * w8 + 3] = wv[w8] & 0xC0C0C0C0u;
+                }
+                ptx::tmem_st_32x32b_x32(tmem + lane_addr + (uint32_t)(aslot * 128 + c * 32), r);
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bars + kBarWEmpty + 8 * wslot);  // stage read: ring slot free
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bars + kBarAFull + 8 * aslot);   // my 32 rows are in TMEM
+        }
+    }
+
+    // ------------------------------------------------------------- epilogue
+    // The CTA barrier orders the staging warps' per-row scales (xmax) before
+    // the epilogue reads them.
+    __syncwarp();
+    __syncthreads();
+    float acc[8];
+#pragma unroll
+    for (int n = 0; n < 8; ++n) acc[n] = 0.f;
+    const bool epi = (warp >= kFirstDecWarp && warp < kFirstDecWarp + 4);  // warpgroup 0 reads D
+    const int quad = warp & 3;
+    const int i = quad * 32 + lane;
+    if (epi && n_chunks > 0) {
+        float dsum[16];
+#pragma unroll
+        for (int n = 0; n < 16; ++n) dsum[n] = 0.f;
+        if (waiter.wait(bars + kBarDFull, 0)) {
+            ptx::tc_fence_after();
+            const uint32_t written = words[2];
+            for (int a = 0; a < kIssuers; ++a) {
+                if (!((written >> a) & 1u)) continue;
+                uint32_t d[16];
+                ptx::tmem_ld_32x32b_x16(tmem + ((uint32_t)(quad * 32) << 16) + kDCol + 16u * a, d);
+                ptx::tmem_wait_ld();
+#pragma unroll
+                for (int n = 0; n < 16; ++n) dsum[n] += __uint_as_float(d[n]);
+            }
+        }
+#pragma unroll
+        for (int mm = 0; mm < 8; ++mm) {
+            if (mm < m) {
+                const uint32_t mb = xmax[mm];
+                const int e = mb == 0 ? 0 : (int)(mb >> 23) - 127;
+                const int s = min(max(7 - e, -120), 120);
+                acc[mm] = dsum[2 * mm] * exp2i(-s) + dsum[2 * mm + 1] * exp2i(-s - 4 < -126 ? -126 : -s - 4);
+            }
+        }
+    }
+    ptx::tc_fence_before();
+    if (split > 1) {
+        // every rank pushes its partial into rank 0's buffer slot [rank]; one
+        // cluster barrier; rank 0 sums the slots in rank order
+        if (epi) {
+            const uint32_t dst = ptx::mapa(ptx::smem_u32(red + ((size_t)rank * 128 + i) * 8), 0u);
+            ptx::st_cluster_v4(dst, acc[0], acc[1], acc[2], acc[3]);
+            ptx::st_cluster_v4(dst + 16u, acc[4], acc[5], acc[6], acc[7]);
+        }
+        ptx::cluster_arrive();
+        ptx::cluster_wait();
+        if (epi && rank == 0) {
+#pragma unroll
+            for (int n = 0; n < 8; ++n) acc[n] = 0.f;
+            for (int r = 0; r < split; ++r) {
+                const float4 a = *reinterpret_cast<const float4 *>(red + ((size_t)r * 128 + i) * 8);
+                const float4 b = *reinterpret_cast<const float4 *>(red + ((size_t)r * 128 + i) * 8 + 4);
+                acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
+                acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+            }
+        }
+    }
+    if (rank == 0 && epi) {
+        if constexpr (SWIGLU) {
+            const int r = row0 + (i & 63);
+            if (i >= 64 && r < p.rows) {
+                const float su = p.scale_u[r];
+#pragma unroll
+                for (int n = 0; n < 8; ++n) xch[(i - 64) * 8 + n] = su * (0.5f * acc[n]);
+            }
+            ptx::named_bar_sync(1, 128);
+            if (i < 64 && r < p.rows) {
+                const float sg = p.scale_g[r];
+#pragma unroll
+                for (int n = 0; n < 8; ++n) {
+                    if (n < m) {
+                        const float gv = sg * (0.5f * acc[n]);
+                        p.y[(size_t)n * p.rows + r] = silu_f(gv) * xch[i * 8 + n];
+                    }
+                }
+            }
+        } else {
+            const int r = row0 + i;
+            if (r < p.rows) {
+                const float sc = p.scale_g[r];
+#pragma unroll
+                for (int n = 0; n < 8; ++n)
+                    if (n < m) p.y[(size_t)n * p.rows + r] = sc * (0.5f * acc[n]);
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        // On an abort path MMAs may still be in flight: wait (bounded) for
+        // their commits before the tensor memory is released.
+        if (lane == 0) drain_wait(bars + kBarDFull, 0);
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiled encode_fn()
+{
+    static EncodeTiled fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    }
+    return fn;
+}
+
+// rows x kw uint32 words, box = 32 words x box_rows rows, 128-byte swizzle.
+bool make_map(CUtensorMap *m, const uint32_t *codes, int rows, int kw, int box_rows)
+{
+    EncodeTiled fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)kw, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kw * 4};
+    const cuuint32_t box[2] = {(cuuint32_t)kStageWords, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t *>(codes), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool SWIGLU>
+tern_status launch_mma(const tern_matrix *g, const tern_matrix *u, const uint16_t *x, int m, float *y,
+                       cudaStream_t stream)
+{
+    const int rows = g->rows, k = g->k, kw = k / 16;
+    const int tile_rows = SWIGLU ? 64 : 128;
+    const int tiles = (rows + tile_rows - 1) / tile_rows;
+    const int total_st = (kw + kStageWords - 1) / kStageWords;
+    const int sms = sm_count();
+
+    int split = 1;
+    while (split < 8 && tiles * split * 2 <= sms && split * 2 <= total_st) split *= 2;
+    const uint32_t misc = 8 * 128 * 8 * 4 + 64 * 8 * 4 + kBarBytes + 64;
+    int per_st = 0, n_wst = 0;
+    for (;;) {
+        per_st = total_st > 0 ? (total_st + split - 1) / split : 0;
+        const uint32_t fixed = 1024 + (uint32_t)per_st * kStageWords * kBBytesPerWord + misc;
+        n_wst = fixed < (uint32_t)kSmemLimit ? (int)((kSmemLimit - fixed) / kStageBytes) : 0;
+        if (n_wst > kMaxWStages) n_wst = kMaxWStages;
+        if (n_wst > per_st && per_st >= 1) n_wst = per_st < 2 ? 2 : per_st;  // no deeper than the work
+        if (n_wst >= 2 || split >= 8) break;
+        split *= 2;
+    }
+    if (n_wst < 2) return TERN_ERR_SHAPE;
+
+    MmaParams prm;
+    prm.scale_g = g->scale;
+    prm.scale_u = SWIGLU ? u->scale : nullptr;
+    prm.x = x;
+    prm.y = y;
+    prm.rows = rows;
+    prm.k = k;
+    prm.m = m;
+    prm.total_st = total_st;
+    prm.per_st = per_st;
+    prm.split = split;
+    prm.n_wst = n_wst;
+    prm.off_b = (uint32_t)n_wst * kStageBytes;
+    prm.off_red = prm.off_b + (uint32_t)per_st * kStageWords * kBBytesPerWord;
+    prm.off_xch = prm.off_red + (uint32_t)split * 128 * 8 * 4;
+    prm.off_bar = prm.off_xch + 64 * 8 * 4;
+    uint32_t smem = 1024 + prm.off_bar + kBarBytes;
+    if (smem < kMinSmem) smem = kMinSmem;
+
+    CUtensorMap tg, tu;
+    std::memset(&tg, 0, sizeof(tg));
+    std::memset(&tu, 0, sizeof(tu));
+    if (kw > 0) {
+        if (!make_map(&tg, g->codes, rows, kw, tile_rows)) return TERN_ERR_CUDA;
+        if (SWIGLU && !make_map(&tu, u->codes, rows, kw, tile_rows)) return TERN_ERR_CUDA;
+    }
+
+    auto kern = k_tern_mma<SWIGLU>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+        return TERN_ERR_CUDA;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(tiles * split), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (split > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = (unsigned)split;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    if (cudaLaunchKernelEx(&cfg, kern, tg, tu, prm) != cudaSuccess) return TERN_ERR_CUDA;
+    return cudaGetLastError() == cudaSuccess ? TERN_OK : TERN_ERR_CUDA;
+}
+
+}  // namespace
+
+tern_status gemm_mma(const tern_matrix *g, const tern_matrix *u, const uint16_t *x, int m, float *y,
+                     cudaStream_t s)
+{
+    if (m < 1 || m > 8) return TERN_ERR_M_RANGE;
+    return u ? launch_mma<true>(g, u, x, m, y, s) : launch_mma<false>(g, nullptr, x, m, y, s);
+}
+
+tern_status take_mma_error()
+{
+    unsigned int v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_mma_error, sizeof(v)) != cudaSuccess) return TERN_ERR_CUDA;
+    if (v != 0u) {
+        if (cudaMemcpyToSymbol(g_mma_error, &z, sizeof(z)) != cudaSuccess) return TERN_ERR_CUDA;
+        return TERN_ERR_TIMEOUT;
+    }
+    return TERN_OK;
+}
+
+}  // namespace tern
