@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--api", default="batched", choices=["batched", "single"],
+                    help="batched: one persistent tern_gemm_batched launch per step; single: one launch per call")
     return ap.parse_args()
 
 
@@ -303,17 +305,26 @@ def run_ours(args, dist: Dist):
     tern.load()
     wl = workloads.build(args.workload, device=dev, seed_offset=dist.rank)
     ncalls = len(wl.calls)
+    launches_per_step = (-(-ncalls // 48)) if args.api == "batched" else ncalls
     stream = torch.cuda.Stream(device=dev)
+
+    batch = workloads.batch_of(wl.calls) if args.api == "batched" else None
+
+    def step_fn():
+        if batch is not None:
+            workloads.run_batched(batch, stream)
+        else:
+            workloads.run_calls(wl.calls, stream)
 
     # one eager pass (sets kernel attributes), then capture the step in a graph
     with torch.cuda.stream(stream):
-        workloads.run_calls(wl.calls, stream)
+        step_fn()
     stream.synchronize()
     if tern.tern_last_device_error(stream) != tern.TERN_OK:
         raise SystemExit("device error after the first pass")
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream):
-        workloads.run_calls(wl.calls, stream)
+        step_fn()
     torch.cuda.synchronize()
 
     with torch.cuda.stream(stream):
@@ -347,14 +358,14 @@ def run_ours(args, dist: Dist):
     step_ms = ms_max / args.steps
     value = dist.world * packed * args.steps / (ms_max * 1e-3) / 1e9
     us_per_call = 1e3 * step_ms / ncalls
-    per_launch_s = ms * 1e-3 / (args.steps * ncalls)
-    achieved = (alg / ncalls) / per_launch_s / 1e9
+    per_launch_s = ms * 1e-3 / (args.steps * launches_per_step)
+    achieved = (alg / launches_per_step) / per_launch_s / 1e9
     peak, peak_kind = peaks()
     traffic, traffic_kernel = ncu_traffic(args.workload)
 
     e2e = None
     if not args.no_e2e:
-        e2e = run_e2e(args, wl, stream, dist)
+        e2e = run_e2e(args, wl, stream, dist, batch)
 
     cpu = None
     if dist.rank == 0 and not args.no_cpu_baseline:
@@ -371,14 +382,16 @@ def run_ours(args, dist: Dist):
                    "distinct_draws": wl.distinct, "packed_bytes_per_step": packed,
                    "algorithmic_bytes_per_step": alg, "us_per_call": round(us_per_call, 4),
                    "l2": "inputs larger than L2: each step streams %.0f MB of distinct buffers" % (packed / 1e6),
-                   "graph": "one CUDA graph per step, replayed", "parallelism": f"replicas x{dist.world}"},
+                   "graph": "one CUDA graph per step, replayed", "parallelism": f"replicas x{dist.world}",
+                   "api": ("tern_gemm_batched: one persistent launch per 48 calls" if args.api == "batched"
+                           else "one tern_* launch per call")},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
                      "traffic": traffic, "traffic_kernel": traffic_kernel,
-                     "bytes_per_launch": alg // ncalls},
+                     "bytes_per_launch": alg // launches_per_step},
         "clocks": clk,
-        "gpu_launches": args.steps * ncalls,
+        "gpu_launches": args.steps * launches_per_step,
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
@@ -387,9 +400,10 @@ def run_ours(args, dist: Dist):
     return 0
 
 
-def run_e2e(args, wl, stream, dist: Dist):
-    """Same metric through the public API with host buffers: each call copies
-    its activations from pinned host memory, runs, and copies its output back;
+def run_e2e(args, wl, stream, dist: Dist, batch=None):
+    """Same metric through the public API with host buffers: every step copies
+    each call's activations from pinned host memory, runs the calls (one
+    batched launch, or one launch per call), and copies every output back;
     weights are the resident model."""
     import torch
 
@@ -401,10 +415,17 @@ def run_e2e(args, wl, stream, dist: Dist):
     d2h = sum(t.numel() * t.element_size() for t in hy)
 
     def step():
-        for c, x, y in zip(wl.calls, hx, hy):
-            c.x.copy_(x, non_blocking=True)
-            workloads.run_call(c, stream)
-            y.copy_(c.y, non_blocking=True)
+        if batch is not None:
+            for c, x in zip(wl.calls, hx):
+                c.x.copy_(x, non_blocking=True)
+            workloads.run_batched(batch, stream)
+            for c, y in zip(wl.calls, hy):
+                y.copy_(c.y, non_blocking=True)
+        else:
+            for c, x, y in zip(wl.calls, hx, hy):
+                c.x.copy_(x, non_blocking=True)
+                workloads.run_call(c, stream)
+                y.copy_(c.y, non_blocking=True)
         stream.synchronize()
 
     with torch.cuda.stream(stream):
@@ -418,7 +439,7 @@ def run_e2e(args, wl, stream, dist: Dist):
     dt = dist.max(dt)
     return {"value": round(dist.world * wl.packed_bytes * args.e2e_steps / dt / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-            "how": "per call: pinned H2D of x, tern ABI call, D2H of y; no graph; host-timed"}
+            "how": "per step: pinned H2D of every x, the tern ABI call(s), D2H of every y; no graph; host-timed"}
 
 
 def main():

@@ -142,6 +142,27 @@ TERN_API tern_status tern_gemm_smallm(const tern_matrix *w, const uint16_t *x, i
 TERN_API tern_status tern_gemm_smallm_swiglu(const tern_matrix *gate, const tern_matrix *up,
                                     const uint16_t *x, int32_t m, float *h, void *stream);
 
+/* One item of a batched call: y = W x when up == NULL, or the fused pair
+ * h = silu(W x) * (up x) (W is then the gate), for m activation rows.
+ * Pointers and layouts as for the single calls above. */
+typedef struct {
+    const tern_matrix *w;   /* weights (the gate of a SwiGLU pair) */
+    const tern_matrix *up;  /* NULL, or the up projection of a SwiGLU pair */
+    const uint16_t *x;      /* [m][k] bf16, 16-byte aligned */
+    float *y;               /* [m][rows] fp32 */
+    int32_t m;              /* 1 <= m <= TERN_MAX_M */
+} tern_batch_item;
+
+/* Many independent products in one persistent launch (one CTA per SM
+ * streaming a byte-balanced share of all items' weights): the seven linears
+ * of a layer, the 252 linears of a token, a batch of projections.  Items
+ * must be independent: no item's y may overlap another item's x, y or
+ * weights.  Every item is checked as by the single calls before anything is
+ * launched; the first failing item's status is returned and nothing runs.
+ * Items are launched in groups of up to 48 in order on `stream`.
+ * n == 0 is a no-op; items == NULL gives TERN_ERR_NULL, n < 0 TERN_ERR_SHAPE. */
+TERN_API tern_status tern_gemm_batched(const tern_batch_item *items, int32_t n, void *stream);
+
 /* Synchronise `stream`, then report and clear the device error word that
  * bounded device-side waits set when they run out (TERN_ERR_TIMEOUT), or a
  * pending CUDA error (TERN_ERR_CUDA).  TERN_OK otherwise. */

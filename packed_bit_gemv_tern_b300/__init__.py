@@ -36,7 +36,7 @@ TERN_MAX_M = 8
 
 ABI_FUNCTIONS = (
     "tern_pack", "tern_validate", "tern_unpack", "tern_gemv", "tern_gemv_swiglu",
-    "tern_gemm_smallm", "tern_gemm_smallm_swiglu", "tern_last_device_error",
+    "tern_gemm_smallm", "tern_gemm_smallm_swiglu", "tern_gemm_batched", "tern_last_device_error",
     "tern_status_str", "tern_abi_version",
 )
 
@@ -50,6 +50,11 @@ class TernError(RuntimeError):
 class CMatrix(ctypes.Structure):
     _fields_ = [("rows", ctypes.c_int32), ("k", ctypes.c_int32), ("codes", ctypes.c_void_p),
                 ("scale", ctypes.c_void_p), ("rowsum", ctypes.c_void_p)]
+
+
+class CBatchItem(ctypes.Structure):
+    _fields_ = [("w", ctypes.c_void_p), ("up", ctypes.c_void_p), ("x", ctypes.c_void_p),
+                ("y", ctypes.c_void_p), ("m", ctypes.c_int32)]
 
 
 _lib = None
@@ -76,6 +81,7 @@ def load(path: str | None = None):
             "tern_gemv_swiglu": [vp, vp, vp, vp, vp],
             "tern_gemm_smallm": [vp, vp, i32, vp, vp],
             "tern_gemm_smallm_swiglu": [vp, vp, vp, i32, vp, vp],
+            "tern_gemm_batched": [vp, i32, vp],
             "tern_last_device_error": [vp],
             "tern_status_str": [ctypes.c_int],
             "tern_abi_version": [],
@@ -196,6 +202,27 @@ def tern_gemm_smallm(w: TernMatrix, x, m: int, y, stream=None):
 def tern_gemm_smallm_swiglu(gate: TernMatrix, up: TernMatrix, x, m: int, h, stream=None):
     _check(load().tern_gemm_smallm_swiglu(gate.ref(), up.ref(), _dptr(x), int(m), _dptr(h),
                                           _stream_handle(stream)), "tern_gemm_smallm_swiglu")
+
+
+def batch_items(items):
+    """ctypes array for tern_gemm_batched from (w, up, x, y, m) tuples; up may be None.
+
+    The returned array references the TernMatrix structs, which must stay alive."""
+    arr = (CBatchItem * len(items))()
+    for i, (w, up, x, y, m) in enumerate(items):
+        arr[i].w = ctypes.addressof(w._c)
+        arr[i].up = ctypes.addressof(up._c) if up is not None else None
+        arr[i].x = _dptr(x)
+        arr[i].y = _dptr(y)
+        arr[i].m = int(m)
+    return arr
+
+
+def tern_gemm_batched(items, stream=None):
+    """items: sequence of (w, up, x, y, m) tuples, or an array from batch_items()."""
+    arr = items if isinstance(items, ctypes.Array) else batch_items(items)
+    _check(load().tern_gemm_batched(ctypes.cast(arr, ctypes.c_void_p) if len(arr) else None, len(arr),
+                                    _stream_handle(stream)), "tern_gemm_batched")
 
 
 def tern_last_device_error(stream=None) -> int:

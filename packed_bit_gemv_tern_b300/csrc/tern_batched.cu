@@ -1,0 +1,554 @@
+// tern_batched.cu -- one persistent launch for a batch of independent ternary
+// products: M = 1 GEMVs, small-M GEMMs and fused SwiGLU pairs (Neutrino-1 8B
+// model page: seven coded linears per layer, gate/up feeding a SwiGLU; the
+// speculative verifier's M = 7 pass).
+//
+// Each of the grid's CTAs (one per SM) owns a contiguous run of work units;
+// a unit is one 128-row tile (64 gate + 64 up rows for a SwiGLU pair) of one
+// item over the item's whole K, so no unit needs a cross-CTA reduction.  The
+// host balances the runs by packed bytes.  K is processed in chunks of 4096
+// codes; the B operand (activations as two e4m3 terms under a per-row
+// power-of-two scale, see split_pair) and the fp32 accumulators are double
+// buffered per chunk, so staging the next chunk's activations and reading the
+// previous chunk's sums overlap the weight stream.  Roles (17 warps):
+//   * warp 0, lane 0: TMA producer; streams every stage of every unit of the
+//     CTA through a 5-deep ring of 16 KB stages (128 rows x 512 codes,
+//     128-byte swizzle), never waiting on activations.
+//   * warps 1-4: stage B for each chunk (after griddepcontrol.wait), then read
+//     the previous chunk's accumulators, rescale and add them into per-row
+//     registers, and at the end of a unit write y (scale, SiLU gate).
+//   * warps 5-12: two decoder warpgroups taking alternate stages; codes become
+//     e4m3 +-2/0 bytes (decode8) stored to one of three TMEM stage slots.
+//   * warps 13-16, lane 0: MMA issuers; issuer k runs K=32 steps 4k..4k+3 of
+//     every stage (tcgen05.mma kind::f8f6f4, A from TMEM, B from shared
+//     memory, M = 128, N = 16) into its own accumulator of the chunk's buffer.
+// Every mbarrier wait is bounded; on time-out the kernel records the error,
+// stops, drains its copies and MMAs, releases its tensor memory and returns.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+#include "tern.h"
+#include "tern_internal.cuh"
+#include "tern_mma_common.cuh"
+#include "tern_ptx.cuh"
+
+namespace tern {
+
+namespace {
+
+using namespace mma;
+
+constexpr int kMaxItems = 48;              // items per launch (kernel parameter space)
+constexpr int kMaxCtas = 160;
+constexpr int kThreads = 544;              // 17 warps
+constexpr int kFirstStager = 1;            // warps 1-4
+constexpr int kStagers = 128;
+constexpr int kFirstDec = 5;               // warps 5-12
+constexpr int kFirstIssuer = 13;           // warps 13-16
+constexpr int kIssuers = 4;
+constexpr int kChunkStages = 8;            // K chunk = 8 stages = 4096 codes
+constexpr int kASlots = 3;                 // TMEM A slots, one stage (128 columns) each
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kDCol = kASlots * 128;  // D[buf][k] at kDCol + 16 * (kIssuers * buf + k)
+constexpr int kBBufBytes = kChunkStages * kStageWords * kBBytesPerWord;  // 64 KB per chunk buffer
+constexpr int kWStages = 5;                // weight ring depth
+
+struct Item {
+    const float *scale_g;
+    const float *scale_u;
+    const uint16_t *x;
+    float *y;
+    int rows, k, m, swiglu;
+    int stages;  // 512-code stages over K
+    int unit0;   // first global unit of this item
+};
+
+struct Params {
+    int n_items;
+    int unit_start[kMaxCtas + 1];  // CTA b runs units [unit_start[b], unit_start[b + 1])
+    Item item[kMaxItems];
+};
+
+struct Maps {
+    CUtensorMap m[2 * kMaxItems];  // [2i] plain/gate codes of item i, [2i+1] up codes
+};
+
+// Shared-memory layout (bytes from the 1024-aligned base).
+constexpr uint32_t kOffW = 0;
+constexpr uint32_t kOffB = kOffW + kWStages * kStageBytes;
+constexpr uint32_t kOffXch = kOffB + 2 * kBBufBytes;  // [64][8] fp32
+constexpr uint32_t kOffBar = kOffXch + 64 * 8 * 4;
+constexpr uint32_t kBarWFull = 0;                       // [kWStages]
+constexpr uint32_t kBarWEmpty = kBarWFull + 8 * kWStages;
+constexpr uint32_t kBarAFull = kBarWEmpty + 8 * kWStages;  // [kASlots]
+constexpr uint32_t kBarAEmpty = kBarAFull + 8 * kASlots;
+constexpr uint32_t kBarBFull = kBarAEmpty + 8 * kASlots;   // [2]
+constexpr uint32_t kBarBEmpty = kBarBFull + 16;
+constexpr uint32_t kBarDFull = kBarBEmpty + 16;
+constexpr uint32_t kBarDEmpty = kBarDFull + 16;
+constexpr uint32_t kBarDrain = kBarDEmpty + 16;  // one commit per issuer on exit
+constexpr uint32_t kWordsOff = kBarDrain + 8;
+// words: [0] tmem base, [1] abort, [8..15] xmax buffer 0, [16..23] xmax buffer 1
+constexpr uint32_t kSmemBytes = 1024 + kOffBar + kWordsOff + 32 * 4;
+
+__device__ unsigned int g_batched_error;
+
+// Walks the (unit, chunk, stage) sequence of one CTA.
+struct Cursor {
+    const Params *p;
+    int unit, unit_end, item, tile, chunk, n_chunks, stage_in_chunk, n_stages_chunk;
+    __device__ void set_unit()
+    {
+        item = 0;
+        while (item + 1 < p->n_items && p->item[item + 1].unit0 <= unit) ++item;
+        tile = unit - p->item[item].unit0;
+        chunk = 0;
+        n_chunks = (p->item[item].stages + kChunkStages - 1) / kChunkStages;
+        set_chunk();
+    }
+    __device__ void set_chunk()
+    {
+        stage_in_chunk = 0;
+        n_stages_chunk = min(kChunkStages, p->item[item].stages - chunk * kChunkStages);
+    }
+    __device__ bool begin(const Params *pp, int b)
+    {
+        p = pp;
+        unit = p->unit_start[b];
+        unit_end = p->unit_start[b + 1];
+        if (unit >= unit_end) return false;
+        set_unit();
+        return true;
+    }
+    // Advance one chunk; false at the end of the CTA's run.
+    __device__ bool next_chunk()
+    {
+        if (++chunk < n_chunks) {
+            set_chunk();
+            return true;
+        }
+        if (++unit >= unit_end) return false;
+        set_unit();
+        return true;
+    }
+    __device__ bool last_chunk_of_unit() const { return chunk + 1 == n_chunks; }
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps maps)
+{
+    extern __shared__ unsigned char smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    unsigned char *gbase = smem_raw + (base - raw);
+    const uint32_t wbuf = base + kOffW;
+    const uint32_t bbuf = base + kOffB;
+    float *xch = reinterpret_cast<float *>(gbase + kOffXch);
+    const uint32_t bars = base + kOffBar;
+    uint32_t *words = reinterpret_cast<uint32_t *>(gbase + kOffBar + kWordsOff);
+    volatile uint32_t *abort_flag = words + 1;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    if (tid == 0) {
+        for (int s = 0; s < kWStages; ++s) {
+            ptx::mbar_init(bars + kBarWFull + 8 * s, 1);
+            ptx::mbar_init(bars + kBarWEmpty + 8 * s, 4);
+        }
+        for (int s = 0; s < kASlots; ++s) {
+            ptx::mbar_init(bars + kBarAFull + 8 * s, 4);
+            ptx::mbar_init(bars + kBarAEmpty + 8 * s, kIssuers);
+        }
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(bars + kBarBFull + 8 * b, 4);
+            ptx::mbar_init(bars + kBarBEmpty + 8 * b, kIssuers);
+            ptx::mbar_init(bars + kBarDFull + 8 * b, kIssuers);
+            ptx::mbar_init(bars + kBarDEmpty + 8 * b, 4);
+        }
+        ptx::mbar_init(bars + kBarDrain, kIssuers);
+        for (int j = 1; j < 32; ++j) words[j] = 0u;
+        ptx::fence_proxy_async_smem();
+    }
+    if (warp == 0) {
+        __syncwarp();
+        ptx::tmem_alloc(ptx::smem_u32(words), kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = words[0];
+    if (tid == 0) ptx::grid_dep_launch();
+    const Waiter waiter{abort_flag, &g_batched_error};
+    Cursor cur;
+    const bool any = cur.begin(&p, (int)blockIdx.x);
+
+    if (warp == 0) {
+        // --------------------------------------------------------- producer
+        if (lane == 0 && any) {
+            int gs = 0;
+            bool more = true;
+            while (more) {
+                const Item &it = p.item[cur.item];
+                const int row0 = cur.tile * (it.swiglu ? 64 : 128);
+                for (int st = 0; st < cur.n_stages_chunk; ++st, ++gs) {
+                    const int slot = gs % kWStages;
+                    if (gs >= kWStages && !waiter.wait(bars + kBarWEmpty + 8 * slot, ((gs / kWStages) - 1) & 1)) {
+                        more = false;
+                        break;
+                    }
+                    const uint32_t dst = wbuf + slot * kStageBytes, full = bars + kBarWFull + 8 * slot;
+                    const int c0 = (cur.chunk * kChunkStages + st) * kStageWords;
+                    ptx::mbar_arrive_expect_tx(full, kStageBytes);
+                    if (it.swiglu) {
+                        ptx::tma_load_2d(dst, &maps.m[2 * cur.item], c0, row0, full);
+                        ptx::tma_load_2d(dst + kStageBytes / 2, &maps.m[2 * cur.item + 1], c0, row0, full);
+                    } else {
+                        ptx::tma_load_2d(dst, &maps.m[2 * cur.item], c0, row0, full);
+                    }
+                }
+                more = more && cur.next_chunk();
+            }
+            for (int s = gs > kWStages ? gs - kWStages : 0; s < gs; ++s)
+                drain_wait(bars + kBarWFull + 8 * (s % kWStages), (s / kWStages) & 1, &g_batched_error);
+        }
+    } else if (warp >= kFirstDec && warp < kFirstIssuer) {
+        // --------------------------------------------------------- decoders
+        const int g = (warp - kFirstDec) >> 2;
+        const int quad = warp & 3;
+        const int i = quad * 32 + lane;
+        const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+        const uint32_t row_addr = wbuf + (uint32_t)i * 128u;
+        int gs = 0;
+        bool more = any;
+        while (more) {
+            for (int st = 0; st < cur.n_stages_chunk && more; ++st, ++gs) {
+                if ((gs & 1) != g) continue;
+                const int wslot = gs % kWStages, aslot = gs % kASlots;
+                uint32_t ok = 1u;
+                if (lane == 0) {
+                    ok = waiter.wait(bars + kBarWFull + 8 * wslot, (gs / kWStages) & 1) ? 1u : 0u;
+                    if (ok && gs >= kASlots)
+                        ok = waiter.wait(bars + kBarAEmpty + 8 * aslot, ((gs / kASlots) - 1) & 1) ? 1u : 0u;
+                }
+                if (__shfl_sync(0xFFFFFFFFu, ok, 0) == 0u) {
+                    more = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const uint32_t srow = row_addr + (uint32_t)wslot * kStageBytes;
+#pragma unroll 1
+                for (int c = 0; c < 4; ++c) {
+                    const uint4 v0 = ptx::lds128(srow + ((uint32_t)((2 * c) ^ (i & 7)) << 4));
+                    const uint4 v1 = ptx::lds128(srow + ((uint32_t)((2 * c + 1) ^ (i & 7)) << 4));
+                    uint32_t r[32];
+                    decode8(v0, v1, r);
+                    ptx::tmem_st_32x32b_x32(tmem + lane_addr + (uint32_t)(aslot * 128 + c * 32), r);
+                }
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bars + kBarWEmpty + 8 * wslot);
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bars + kBarAFull + 8 * aslot);
+            }
+            more = more && cur.next_chunk();
+        }
+    } else if (warp >= kFirstIssuer) {
+        // --------------------------------------------------------- MMA issuers
+        const int k_iss = warp - kFirstIssuer;
+        if (lane == 0 && any) {
+            int gs = 0, gc = 0;
+            bool ok = true;
+            while (ok) {
+                const int buf = gc & 1;
+                const uint32_t d = tmem + kDCol + 16u * (uint32_t)(kIssuers * buf + k_iss);
+                ok = waiter.wait(bars + kBarBFull + 8 * buf, (gc >> 1) & 1);
+                if (ok && gc >= 2) ok = waiter.wait(bars + kBarDEmpty + 8 * buf, ((gc >> 1) - 1) & 1);
+                if (!ok) break;
+                ptx::tc_fence_after();
+                const uint32_t bb = bbuf + (uint32_t)buf * kBBufBytes;
+                for (int st = 0; st < cur.n_stages_chunk; ++st, ++gs) {
+                    const int aslot = gs % kASlots;
+                    if (!waiter.wait(bars + kBarAFull + 8 * aslot, (gs / kASlots) & 1)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const int step = 4 * k_iss + t;           // K=32 step within the stage
+                        const int wi = st * kStageWords + 2 * step;  // its first word within the chunk
+                        ptx::mma_ts_f8f6f4(d, tmem + (uint32_t)(aslot * 128 + step * 8),
+                                           b_desc(bb + (uint32_t)wi * kBBytesPerWord), kIdesc,
+                                           (st | t) != 0 ? 1u : 0u);
+                    }
+                    ptx::mma_commit(bars + kBarAEmpty + 8 * aslot);
+                }
+                if (!ok) break;
+                ptx::mma_commit(bars + kBarDFull + 8 * buf);
+                ptx::mma_commit(bars + kBarBEmpty + 8 * buf);
+                ++gc;
+                ok = cur.next_chunk();
+            }
+        }
+        // arrives once every MMA this thread issued has completed (at once if none)
+        if (lane == 0) ptx::mma_commit(bars + kBarDrain);
+    } else {
+        // ------------------------------------------- B staging and epilogue
+        const int st_tid = tid - 32 * kFirstStager;  // 0..127
+        const int quad = warp & 3;
+        const int i = quad * 32 + lane;               // tile row == TMEM lane
+        ptx::grid_dep_wait();
+        float acc[8];
+#pragma unroll
+        for (int n = 0; n < 8; ++n) acc[n] = 0.f;
+        // previous chunk, whose accumulators are read after the next chunk's B is staged
+        int prev_item = -1, prev_tile = 0;
+        bool prev_last = false;
+        int gc = 0;
+        bool ok = any;
+
+        auto epilogue = [&](int e) {  // read chunk e's accumulators, finish the unit if it was its last chunk
+            const int eb = e & 1;
+            uint32_t good = 1u;
+            if (lane == 0) good = waiter.wait(bars + kBarDFull + 8 * eb, (e >> 1) & 1) ? 1u : 0u;
+            good = __shfl_sync(0xFFFFFFFFu, good, 0);
+            float dsum[16];
+#pragma unroll
+            for (int n = 0; n < 16; ++n) dsum[n] = 0.f;
+            if (good) {
+                ptx::tc_fence_after();
+#pragma unroll 1
+                for (int a = 0; a < kIssuers; ++a) {
+                    uint32_t dv[16];
+                    ptx::tmem_ld_32x32b_x16(tmem + ((uint32_t)(quad * 32) << 16) + kDCol + 16u * (kIssuers * eb + a), dv);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int n = 0; n < 16; ++n) dsum[n] += __uint_as_float(dv[n]);
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bars + kBarDEmpty + 8 * eb);
+            const Item &it = p.item[prev_item];
+            const uint32_t *xm = words + 8 + 8 * eb;
+#pragma unroll
+            for (int mm = 0; mm < 8; ++mm) {
+                if (mm < it.m) {
+                    const int s = row_scale_exp(xm[mm]);
+                    acc[mm] += dsum[2 * mm] * exp2i(-s) + dsum[2 * mm + 1] * exp2i(max(-s - 4, -126));
+                }
+            }
+            if (!prev_last) return;
+            if (it.swiglu) {
+                const int r = prev_tile * 64 + (i & 63);
+                if (i >= 64 && r < it.rows) {
+                    const float su = it.scale_u[r];
+#pragma unroll
+                    for (int n = 0; n < 8; ++n) xch[(i - 64) * 8 + n] = su * (0.5f * acc[n]);
+                }
+                ptx::named_bar_sync(1, kStagers);
+                if (i < 64 && r < it.rows) {
+                    const float sg = it.scale_g[r];
+#pragma unroll
+                    for (int n = 0; n < 8; ++n)
+                        if (n < it.m) it.y[(size_t)n * it.rows + r] = silu_f(sg * (0.5f * acc[n])) * xch[i * 8 + n];
+                }
+                ptx::named_bar_sync(1, kStagers);  // xch reusable
+            } else {
+                const int r = prev_tile * 128 + i;
+                if (r < it.rows) {
+                    const float sc = it.scale_g[r];
+#pragma unroll
+                    for (int n = 0; n < 8; ++n)
+                        if (n < it.m) it.y[(size_t)n * it.rows + r] = sc * (0.5f * acc[n]);
+                }
+            }
+#pragma unroll
+            for (int n = 0; n < 8; ++n) acc[n] = 0.f;
+        };
+
+        while (ok) {
+            const int buf = gc & 1;
+            const Item &it = p.item[cur.item];
+            // the MMAs of chunk gc-2 must be done with this B buffer
+            if (gc >= 2 && lane == 0) waiter.wait(bars + kBarBEmpty + 8 * buf, ((gc >> 1) - 1) & 1);
+            uint32_t *xm = words + 8 + 8 * buf;
+            if (st_tid < 8) xm[st_tid] = 0u;
+            // A failed wait has raised the abort flag before this barrier, so
+            // all four staging warps take the same branch after it.
+            ptx::named_bar_sync(1, kStagers);
+            if (*abort_flag) break;
+            const int n_words = cur.n_stages_chunk * kStageWords;
+            const int k0 = cur.chunk * kChunkStages * kStageWords * 16;
+            const int m = it.m;
+            const int n_items = m * n_words;
+            const uint32_t bb = bbuf + (uint32_t)buf * kBBufBytes;
+            constexpr int kBatch = 4;
+            uint4 xa[kBatch], xb[kBatch];
+            const bool resident = n_items <= kStagers * kBatch;
+            auto load_batch = [&](int first) {
+#pragma unroll
+                for (int t = 0; t < kBatch; ++t) {
+                    const int item = first + t * kStagers;
+                    xa[t] = make_uint4(0, 0, 0, 0);
+                    xb[t] = make_uint4(0, 0, 0, 0);
+                    if (item < n_items) {
+                        const int mm = item / n_words, wi = item - mm * n_words;
+                        const int kk = k0 + 16 * wi;
+                        if (kk < it.k) {
+                            const uint4 *src = reinterpret_cast<const uint4 *>(it.x + (size_t)mm * it.k + kk);
+                            xa[t] = src[0];
+                            xb[t] = src[1];
+                        }
+                    }
+                }
+            };
+            for (int first = st_tid; first < n_items; first += kStagers * kBatch) {
+                load_batch(first);
+#pragma unroll
+                for (int t = 0; t < kBatch; ++t) {
+                    const int item = first + t * kStagers;
+                    if (item < n_items) atomicMax(&xm[item / n_words], max_abs16(xa[t], xb[t]));
+                }
+            }
+            ptx::named_bar_sync(1, kStagers);
+            for (int first = st_tid; first < n_items; first += kStagers * kBatch) {
+                if (!resident) load_batch(first);
+#pragma unroll
+                for (int t = 0; t < kBatch; ++t) {
+                    const int item = first + t * kStagers;
+                    if (item >= n_items) break;
+                    const int mm = item / n_words, wi = item - mm * n_words;
+                    uint4 hi4 = make_uint4(0, 0, 0, 0), lo4 = make_uint4(0, 0, 0, 0);
+                    if (k0 + 16 * wi < it.k) split_word(xa[t], xb[t], exp2i(row_scale_exp(xm[mm])), hi4, lo4);
+                    const uint32_t at = bb + (uint32_t)wi * kBBytesPerWord;
+                    ptx::sts128(at + b_row_off(2 * mm), hi4);
+                    ptx::sts128(at + b_row_off(2 * mm + 1), lo4);
+                }
+            }
+            for (int item = st_tid; item < (8 - m) * n_words; item += kStagers) {  // rows n >= 2m are zero
+                const int mm = m + item / n_words, wi = item % n_words;
+                const uint32_t at = bb + (uint32_t)wi * kBBytesPerWord;
+                ptx::sts128(at + b_row_off(2 * mm), make_uint4(0, 0, 0, 0));
+                ptx::sts128(at + b_row_off(2 * mm + 1), make_uint4(0, 0, 0, 0));
+            }
+            ptx::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bars + kBarBFull + 8 * buf);
+            if (gc >= 1) epilogue(gc - 1);
+            prev_item = cur.item;
+            prev_tile = cur.tile;
+            prev_last = cur.last_chunk_of_unit();
+            ++gc;
+            ok = cur.next_chunk();
+        }
+        if (gc >= 1 && !*abort_flag) epilogue(gc - 1);
+    }
+
+    __syncthreads();
+    if (warp == 0) {
+        // every MMA of this CTA has completed before its tensor memory is released
+        if (lane == 0) drain_wait(bars + kBarDrain, 0, &g_batched_error);
+        __syncwarp();
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t stream)
+{
+    static_assert(sizeof(Params) + sizeof(Maps) < 32000, "kernel parameters exceed 32 KB");
+    const int sms = sm_count();
+    for (int begin = 0; begin < n;) {
+        // one launch covers up to kMaxItems items with rows > 0 and k > 0
+        Params prm;
+        std::memset(&prm, 0, sizeof(prm));
+        Maps maps;
+        std::memset(&maps, 0, sizeof(maps));
+        std::vector<long long> unit_cost;
+        int cnt = 0, idx = begin;
+        int units = 0;
+        for (; idx < n && cnt < kMaxItems; ++idx) {
+            const tern_batch_item &b = items[idx];
+            if (b.w->rows == 0) continue;
+            if (b.w->k == 0) {  // empty sum: y = scale * 0
+                const tern_status st = gemm_cc(b.w, b.up, b.x, b.m, b.y, stream);
+                if (st != TERN_OK) return st;
+                continue;
+            }
+            Item &it = prm.item[cnt];
+            it.scale_g = b.w->scale;
+            it.scale_u = b.up ? b.up->scale : nullptr;
+            it.x = b.x;
+            it.y = b.y;
+            it.rows = b.w->rows;
+            it.k = b.w->k;
+            it.m = b.m;
+            it.swiglu = b.up != nullptr;
+            it.stages = (it.k / 16 + kStageWords - 1) / kStageWords;
+            it.unit0 = units;
+            const int tile_rows = it.swiglu ? 64 : 128;
+            const int tiles = (it.rows + tile_rows - 1) / tile_rows;
+            if (!make_code_map(&maps.m[2 * cnt], b.w->codes, it.rows, it.k / 16, tile_rows)) return TERN_ERR_CUDA;
+            if (it.swiglu && !make_code_map(&maps.m[2 * cnt + 1], b.up->codes, it.rows, it.k / 16, tile_rows))
+                return TERN_ERR_CUDA;
+            for (int t = 0; t < tiles; ++t) unit_cost.push_back(it.stages);
+            units += tiles;
+            ++cnt;
+        }
+        begin = idx;
+        if (cnt == 0) continue;
+        prm.n_items = cnt;
+        // contiguous runs of units with balanced stage counts
+        const int ctas = units < sms ? units : (sms < kMaxCtas ? sms : kMaxCtas);
+        long long total = 0;
+        for (long long c : unit_cost) total += c;
+        int u = 0;
+        long long acc = 0;
+        prm.unit_start[0] = 0;
+        for (int b = 1; b < ctas; ++b) {
+            const long long target = total * b / ctas;
+            while (u < units && acc + unit_cost[u] / 2 < target) acc += unit_cost[u++];
+            prm.unit_start[b] = u;
+        }
+        prm.unit_start[ctas] = units;
+
+        if (cudaFuncSetAttribute(k_tern_batched, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+            cudaSuccess)
+            return TERN_ERR_CUDA;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+        cfg.blockDim = dim3(kThreads, 1, 1);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr.val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, k_tern_batched, prm, maps) != cudaSuccess) return TERN_ERR_CUDA;
+        if (cudaGetLastError() != cudaSuccess) return TERN_ERR_CUDA;
+    }
+    return TERN_OK;
+}
+
+tern_status take_batched_error()
+{
+    unsigned int v = 0, z = 0;
+    if (cudaMemcpyFromSymbol(&v, g_batched_error, sizeof(v)) != cudaSuccess) return TERN_ERR_CUDA;
+    if (v != 0u) {
+        if (cudaMemcpyToSymbol(g_batched_error, &z, sizeof(z)) != cudaSuccess) return TERN_ERR_CUDA;
+        return TERN_ERR_TIMEOUT;
+    }
+    return TERN_OK;
+}
+
+}  // namespace tern

@@ -319,6 +319,24 @@ extern "C" tern_status tern_gemm_smallm_swiglu(const tern_matrix *gate, const te
     return swiglu_dispatch(gate, up, x, m, h, (cudaStream_t)stream);
 }
 
+extern "C" tern_status tern_gemm_batched(const tern_batch_item *items, int32_t n, void *stream)
+{
+    if (n < 0) return TERN_ERR_SHAPE;
+    if (n == 0) return TERN_OK;
+    if (items == nullptr) return TERN_ERR_NULL;
+    for (int32_t i = 0; i < n; ++i) {
+        const tern_batch_item &b = items[i];
+        if (b.up == nullptr) {
+            const tern_status st = check_gemm_args(b.w, nullptr, b.x, b.m, b.y);
+            if (st != TERN_OK) return st;
+        } else {
+            const tern_status st = check_gemm_args(b.w, b.up, b.x, b.m, b.y);
+            if (st != TERN_OK) return st;
+        }
+    }
+    return batched_dispatch(items, n, (cudaStream_t)stream);
+}
+
 extern "C" tern_status tern_last_device_error(void *stream)
 {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return TERN_ERR_CUDA;

@@ -45,6 +45,23 @@ tern_status smallm_dispatch(const tern_matrix *w, const uint16_t *x, int m, floa
     return run(w, nullptr, x, m, y, s);
 }
 
-tern_status take_device_error() { return take_mma_error(); }
+tern_status batched_dispatch(const tern_batch_item *items, int n, cudaStream_t s)
+{
+    if (use_cuda_core()) {
+        for (int i = 0; i < n; ++i) {
+            const tern_status st = gemm_cc(items[i].w, items[i].up, items[i].x, items[i].m, items[i].y, s);
+            if (st != TERN_OK) return st;
+        }
+        return TERN_OK;
+    }
+    return gemm_batched(items, n, s);
+}
+
+tern_status take_device_error()
+{
+    const tern_status a = take_mma_error();
+    const tern_status b = take_batched_error();
+    return a != TERN_OK ? a : b;
+}
 
 }  // namespace tern

@@ -23,11 +23,20 @@ tern_status gemm_mma(const tern_matrix *g, const tern_matrix *u, const uint16_t 
                      cudaStream_t s);
 tern_status take_mma_error();
 
+// Persistent batched kernel (tern_batched.cu); items already checked.
+tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t s);
+tern_status take_batched_error();
+
+// Shared argument checks (tern_cuda.cu).
+tern_status check_gemm_args(const tern_matrix *g, const tern_matrix *u, const uint16_t *x, int32_t m,
+                            const float *y);
+
 // Kernel choice per entry point (tern_dispatch.cu).
 tern_status gemv_dispatch(const tern_matrix *w, const uint16_t *x, float *y, cudaStream_t s);
 tern_status swiglu_dispatch(const tern_matrix *g, const tern_matrix *u, const uint16_t *x, int m,
                             float *h, cudaStream_t s);
 tern_status smallm_dispatch(const tern_matrix *w, const uint16_t *x, int m, float *y, cudaStream_t s);
+tern_status batched_dispatch(const tern_batch_item *items, int n, cudaStream_t s);
 
 // Reads and clears every device error word (TERN_OK when all are clear).
 tern_status take_device_error();

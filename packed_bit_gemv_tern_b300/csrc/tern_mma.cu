@@ -52,6 +52,7 @@
 
 #include "tern.h"
 #include "tern_internal.cuh"
+#include "tern_mma_common.cuh"
 #include "tern_ptx.cuh"
 
 namespace tern {
@@ -63,24 +64,16 @@ constexpr int kStagerWarps = 4;           // warps 1-4: B operand staging, then 
 constexpr int kStagers = 32 * kStagerWarps;
 constexpr int kIssuers = kStagerWarps;    // one MMA issuer (lane 0) per staging warp
 constexpr int kFirstDecWarp = 1 + kStagerWarps;  // warps 5-12: decoders (two warpgroups)
-constexpr int kStageWords = 32;           // words per row per stage (512 codes, 128 B)
-constexpr int kStageBytes = 128 * 128;    // 128 rows x 128 B
 constexpr int kChunkWords = 8;            // words per row per decode chunk (2 x 16 B)
-constexpr int kBBytesPerWord = 256;       // B operand: 16 rows x 16 e4m3 per word
 constexpr int kASlots = 3;                // TMEM A slots, one stage (128 columns) each
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol = kASlots * 128;  // accumulators D[k], k < kIssuers, at [kDCol, kDCol + 16 kIssuers)
 constexpr int kMaxWStages = 8;
-constexpr int kSmemLimit = 227 * 1024;
 // Every CTA allocates all 512 TMEM columns.  Asking for more than half of the
 // SM's shared memory keeps one CTA per SM, so tcgen05.alloc never waits for a
 // CTA of the same launch (which could itself be waiting, at a cluster barrier,
 // on the one that waits).
 constexpr uint32_t kMinSmem = 118 * 1024;
-
-// Instruction descriptor: kind::f8f6f4, D fp32, A e4m3, B e4m3, K-major A and
-// B, N = 16, M = 128.
-constexpr uint32_t kIdesc = (1u << 4) | (0u << 7) | (0u << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
 
 __device__ unsigned int g_mma_error;  // bit 0: a bounded wait ran out
 
@@ -113,76 +106,7 @@ constexpr uint32_t kWords = kBarDFull + 8;                          // uint32 sc
 // words: [0] tmem base, [1] abort, [2] bit mask of written accumulators, [4..11] max|x| bits per row
 constexpr uint32_t kBarBytes = kWords + 16 * 4;
 
-// Shared-memory descriptor of a K-major, unswizzled operand made of 8-row x
-// 16-byte core matrices: adjacent core matrices along K are 256 B apart (LBO),
-// along N 128 B apart (SBO).
-__device__ __forceinline__ uint64_t b_desc(uint32_t addr)
-{
-    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)(256u >> 4) << 16) | ((uint64_t)(128u >> 4) << 32) |
-           (1ull << 46);
-}
-
-struct Waiter {
-    volatile uint32_t *abort_flag;  // shared
-    __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity)
-    {
-        if (*abort_flag) return false;
-        const long long t0 = clock64();
-        uint32_t spins = 0;
-        while (!ptx::mbar_try_wait(bar, parity)) {
-            if ((++spins & 15u) == 0u) {
-                if (*abort_flag) return false;
-                if (clock64() - t0 > (1ll << 31)) {  // ~1 s at 2 GHz
-                    atomicOr(&g_mma_error, 1u);
-                    *abort_flag = 1u;
-                    return false;
-                }
-            }
-        }
-        return true;
-    }
-};
-
-// Bounded wait that ignores the abort flag (used to drain in-flight work).
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity)
-{
-    const long long t0 = clock64();
-    while (!ptx::mbar_try_wait(bar, parity)) {
-        if (clock64() - t0 > (1ll << 31)) {
-            atomicOr(&g_mma_error, 1u);
-            return;
-        }
-    }
-}
-
-__device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
-
-// 2^e as an fp32 (e in [-126, 127]).
-__device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
-
-// Splits a pair of bf16 activations (one 32-bit word, low half = even k)
-// scaled by sc = 2^s into e4m3 bytes with x*2^s = hi + lo/16: hi is x*2^s
-// rounded to nearest e4m3, lo = (x*2^s - hi)*16 rounded to nearest e4m3 (the
-// difference is formed exactly in f16).  For x*2^s >= 2^-6 hi keeps 4
-// significant bits and lo the remaining <= 4, so the pair is exact whenever lo
-// is an e4m3 normal or zero; below that both round to e4m3 subnormals (steps
-// of 2^-9), bounding the error by 2^-14 in units of x*2^s.
-// Output: hp/lp = two bytes each, low byte for the even k.
-__device__ __forceinline__ void split_pair(uint32_t v, float sc, uint32_t &hp, uint32_t &lp)
-{
-    const float xa = __uint_as_float(v << 16) * sc;
-    const float xb = __uint_as_float(v & 0xFFFF0000u) * sc;
-    uint16_t h, l;
-    uint32_t xh, hh, d;
-    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(h) : "f"(xb), "f"(xa));
-    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(hh) : "h"(h));
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(xh) : "f"(xb), "f"(xa));
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(xh), "r"(hh));
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(d), "r"(0x4C004C00u));  // x16
-    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(l) : "r"(d));
-    hp = h;
-    lp = l;
-}
+using namespace mma;
 
 template <bool SWIGLU>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -260,7 +184,7 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
     ptx::tc_fence_after();
     const uint32_t tmem = words[0];
     if (tid == 0) ptx::grid_dep_launch();
-    Waiter waiter{abort_flag};
+    const Waiter waiter{abort_flag, &g_mma_error};
 
     if (warp == 0) {
         // ----------------------------------------------------------- producer
@@ -272,7 +196,7 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
             }
             // every issued copy must land before the CTA may exit
             for (int s = (issued > n_wst ? issued - n_wst : 0); s < issued; ++s)
-                drain_wait(bars + kBarWFull + 8 * (s % n_wst), (s / n_wst) & 1);
+                drain_wait(bars + kBarWFull + 8 * (s % n_wst), (s / n_wst) & 1, &g_mma_error);
         }
     } else if (warp <= kStagerWarps) {
         // ------------------------------------------------- B operand staging
@@ -312,13 +236,7 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
 #pragma unroll
             for (int t = 0; t < kStageItems; ++t) {
                 const int item = first + t * kStagers;
-                if (item < n_items) {
-                    const uint32_t v[8] = {xa[t].x, xa[t].y, xa[t].z, xa[t].w, xb[t].x, xb[t].y, xb[t].z, xb[t].w};
-                    uint32_t mx = 0;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) mx = max(mx, max((v[q] << 16) & 0x7FFF0000u, v[q] & 0x7FFF0000u));
-                    atomicMax(&xmax[item / n_words], mx);
-                }
+                if (item < n_items) atomicMax(&xmax[item / n_words], max_abs16(xa[t], xb[t]));
             }
         }
         ptx::named_bar_sync(3, kStagers);
@@ -330,37 +248,18 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
                 if (item >= n_items) break;
                 const int mm = item / n_words, wi = item - mm * n_words;
                 uint4 hi4 = make_uint4(0, 0, 0, 0), lo4 = make_uint4(0, 0, 0, 0);
-                if (k0 + 16 * wi < p.k) {
-                    const uint32_t mb = xmax[mm];
-                    const int e = mb == 0 ? 0 : (int)(mb >> 23) - 127;
-                    const float sc = exp2i(min(max(7 - e, -120), 120));
-                    const uint32_t v[8] = {xa[t].x, xa[t].y, xa[t].z, xa[t].w, xb[t].x, xb[t].y, xb[t].z, xb[t].w};
-                    uint32_t hp[8], lp[8];  // per k pair: two e4m3 bytes (low byte = even k)
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) split_pair(v[q], sc, hp[q], lp[q]);
-                    // byte b of output word j holds k offset 4b + j (a 4x4 transpose)
-                    const uint32_t h02 = hp[0] | (hp[2] << 16), h46 = hp[4] | (hp[6] << 16);
-                    const uint32_t h13 = hp[1] | (hp[3] << 16), h57 = hp[5] | (hp[7] << 16);
-                    const uint32_t l02 = lp[0] | (lp[2] << 16), l46 = lp[4] | (lp[6] << 16);
-                    const uint32_t l13 = lp[1] | (lp[3] << 16), l57 = lp[5] | (lp[7] << 16);
-                    hi4 = make_uint4(__byte_perm(h02, h46, 0x6420), __byte_perm(h02, h46, 0x7531),
-                                     __byte_perm(h13, h57, 0x6420), __byte_perm(h13, h57, 0x7531));
-                    lo4 = make_uint4(__byte_perm(l02, l46, 0x6420), __byte_perm(l02, l46, 0x7531),
-                                     __byte_perm(l13, l57, 0x6420), __byte_perm(l13, l57, 0x7531));
-                }
-                const int nh = 2 * mm, nl = 2 * mm + 1;  // B rows of the two pieces
+                if (k0 + 16 * wi < p.k) split_word(xa[t], xb[t], exp2i(row_scale_exp(xmax[mm])), hi4, lo4);
                 const uint32_t at = bbuf + (uint32_t)wi * kBBytesPerWord;
-                ptx::sts128(at + (uint32_t)((nh >> 3) * 128 + (nh & 7) * 16), hi4);
-                ptx::sts128(at + (uint32_t)((nl >> 3) * 128 + (nl & 7) * 16), lo4);
+                ptx::sts128(at + b_row_off(2 * mm), hi4);
+                ptx::sts128(at + b_row_off(2 * mm + 1), lo4);
             }
         }
         // rows n >= 2m of B are zero
         for (int item = st_tid; item < (8 - m) * n_words; item += kStagers) {
             const int mm = m + item / n_words, wi = item % n_words;
             const uint32_t at = bbuf + (uint32_t)wi * kBBytesPerWord;
-            const int nh = 2 * mm, nl = 2 * mm + 1;
-            ptx::sts128(at + (uint32_t)((nh >> 3) * 128 + (nh & 7) * 16), make_uint4(0, 0, 0, 0));
-            ptx::sts128(at + (uint32_t)((nl >> 3) * 128 + (nl & 7) * 16), make_uint4(0, 0, 0, 0));
+            ptx::sts128(at + b_row_off(2 * mm), make_uint4(0, 0, 0, 0));
+            ptx::sts128(at + b_row_off(2 * mm + 1), make_uint4(0, 0, 0, 0));
         }
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive(bars + kBarBReady);
@@ -414,15 +313,8 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
             for (int c = 0; c < 4; ++c) {
                 const uint4 v0 = ptx::lds128(srow + ((uint32_t)((2 * c) ^ (i & 7)) << 4));
                 const uint4 v1 = ptx::lds128(srow + ((uint32_t)((2 * c + 1) ^ (i & 7)) << 4));
-                const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
                 uint32_t r[32];
-#pragma unroll
-                for (int w8 = 0; w8 < 8; ++w8) {
-                    r[4 * w8 + 0] = (wv[w8] << 6) & 0xC0C0C0C0u;
-                    r[4 * w8 + 1] = (wv[w8] << 4) & 0xC0C0C0C0u;
-                    r[4 * w8 + 2] = (wv[w8] << 2) & 0xC0C0C0C0u;
-                    r[4 * w8 + 3] = wv[w8] & 0xC0C0C0C0u;
-                }
+                decode8(v0, v1, r);
                 ptx::tmem_st_32x32b_x32(tmem + lane_addr + (uint32_t)(aslot * 128 + c * 32), r);
             }
             __syncwarp();
@@ -464,10 +356,8 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
 #pragma unroll
         for (int mm = 0; mm < 8; ++mm) {
             if (mm < m) {
-                const uint32_t mb = xmax[mm];
-                const int e = mb == 0 ? 0 : (int)(mb >> 23) - 127;
-                const int s = min(max(7 - e, -120), 120);
-                acc[mm] = dsum[2 * mm] * exp2i(-s) + dsum[2 * mm + 1] * exp2i(-s - 4 < -126 ? -126 : -s - 4);
+                const int s = row_scale_exp(xmax[mm]);
+                acc[mm] = dsum[2 * mm] * exp2i(-s) + dsum[2 * mm + 1] * exp2i(max(-s - 4, -126));
             }
         }
     }
@@ -526,7 +416,7 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
     if (warp == 0) {
         // On an abort path MMAs may still be in flight: wait (bounded) for
         // their commits before the tensor memory is released.
-        if (lane == 0) drain_wait(bars + kBarDFull, 0);
+        if (lane == 0) drain_wait(bars + kBarDFull, 0, &g_mma_error);
         __syncwarp();
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kTmemCols);
@@ -534,40 +424,6 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
 }
 
 // ---------------------------------------------------------------- host side
-
-using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiled encode_fn()
-{
-    static EncodeTiled fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiled>(p);
-    }
-    return fn;
-}
-
-// rows x kw uint32 words, box = 32 words x box_rows rows, 128-byte swizzle.
-bool make_map(CUtensorMap *m, const uint32_t *codes, int rows, int kw, int box_rows)
-{
-    EncodeTiled fn = encode_fn();
-    if (fn == nullptr) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)kw, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)kw * 4};
-    const cuuint32_t box[2] = {(cuuint32_t)kStageWords, (cuuint32_t)box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t *>(codes), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 template <bool SWIGLU>
 tern_status launch_mma(const tern_matrix *g, const tern_matrix *u, const uint16_t *x, int m, float *y,
@@ -617,8 +473,8 @@ tern_status launch_mma(const tern_matrix *g, const tern_matrix *u, const uint16_
     std::memset(&tg, 0, sizeof(tg));
     std::memset(&tu, 0, sizeof(tu));
     if (kw > 0) {
-        if (!make_map(&tg, g->codes, rows, kw, tile_rows)) return TERN_ERR_CUDA;
-        if (SWIGLU && !make_map(&tu, u->codes, rows, kw, tile_rows)) return TERN_ERR_CUDA;
+        if (!make_code_map(&tg, g->codes, rows, kw, tile_rows)) return TERN_ERR_CUDA;
+        if (SWIGLU && !make_code_map(&tu, u->codes, rows, kw, tile_rows)) return TERN_ERR_CUDA;
     }
 
     auto kern = k_tern_mma<SWIGLU>;
@@ -649,6 +505,43 @@ tern_status launch_mma(const tern_matrix *g, const tern_matrix *u, const uint16_
 }
 
 }  // namespace
+
+namespace mma {
+
+using EncodeTiled = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                 const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiled encode_fn()
+{
+    static EncodeTiled fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiled>(p);
+    }
+    return fn;
+}
+
+bool make_code_map(CUtensorMap *m, const uint32_t *codes, int rows, int kw, int box_rows)
+{
+    EncodeTiled fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)kw, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kw * 4};
+    const cuuint32_t box[2] = {(cuuint32_t)kStageWords, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t *>(codes), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace mma
 
 tern_status gemm_mma(const tern_matrix *g, const tern_matrix *u, const uint16_t *x, int m, float *y,
                      cudaStream_t s)

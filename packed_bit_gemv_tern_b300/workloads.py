@@ -10,7 +10,8 @@ import dataclasses
 
 import numpy as np
 
-from . import TernMatrix, synth, tern_gemm_smallm, tern_gemm_smallm_swiglu, tern_gemv, tern_gemv_swiglu, tern_pack
+from . import (TernMatrix, batch_items, synth, tern_gemm_batched, tern_gemm_smallm, tern_gemm_smallm_swiglu, tern_gemv,
+               tern_gemv_swiglu, tern_pack)
 
 MiB = 1 << 20
 
@@ -56,8 +57,19 @@ def run_call(c: Call, stream=None):
 
 
 def run_calls(calls, stream=None):
+    """Issue every call of a step as its own single-call launch."""
     for c in calls:
         run_call(c, stream)
+
+
+def batch_of(calls):
+    """The calls of a step as one tern_gemm_batched item array (independent items)."""
+    return batch_items([(c.w, c.up, c.x, c.y, c.m) for c in calls])
+
+
+def run_batched(batch, stream=None):
+    """Issue a step through the persistent batched entry point."""
+    tern_gemm_batched(batch, stream)
 
 
 def _x(rng, m, k, device):

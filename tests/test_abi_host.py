@@ -128,6 +128,22 @@ def test_device_entry_points_reject_before_launch(lib):
     # unpack
     assert lib.tern_unpack(ref(ok_m), None, None) == tern.TERN_ERR_NULL
     assert lib.tern_unpack(ref(ok_m), ctypes.c_void_p(0x5001), None) == tern.TERN_ERR_ALIGN
+    # batched: bad count / NULL array / a bad item rejects the whole batch
+    assert lib.tern_gemm_batched(None, -1, None) == tern.TERN_ERR_SHAPE
+    assert lib.tern_gemm_batched(None, 0, None) == tern.TERN_OK
+    assert lib.tern_gemm_batched(None, 2, None) == tern.TERN_ERR_NULL
+    good = _mat(4, 64)
+    arr = (tern.CBatchItem * 2)()
+    arr[0].w, arr[0].up, arr[0].x, arr[0].y, arr[0].m = ctypes.addressof(good), None, 0x3000, 0x4000, 1
+    bad = _mat(4, 48)
+    arr[1].w, arr[1].up, arr[1].x, arr[1].y, arr[1].m = ctypes.addressof(bad), None, 0x3000, 0x4000, 1
+    assert lib.tern_gemm_batched(ctypes.cast(arr, ctypes.c_void_p), 2, None) == tern.TERN_ERR_SHAPE
+    arr[1].w, arr[1].m = ctypes.addressof(good), 0
+    assert lib.tern_gemm_batched(ctypes.cast(arr, ctypes.c_void_p), 2, None) == tern.TERN_ERR_M_RANGE
+    arr[1].m, arr[1].up = 1, ctypes.addressof(_mat(5, 64))
+    assert lib.tern_gemm_batched(ctypes.cast(arr, ctypes.c_void_p), 2, None) == tern.TERN_ERR_SHAPE
+    arr[1].up, arr[1].x = None, 0x3004
+    assert lib.tern_gemm_batched(ctypes.cast(arr, ctypes.c_void_p), 2, None) == tern.TERN_ERR_ALIGN
     # empty problems succeed without a launch, with NULL pointers
     empty = tern.CMatrix(0, 64, None, None, None)
     assert lib.tern_gemv(ref(empty), None, None, None) == tern.TERN_OK

@@ -253,3 +253,72 @@ def test_sweep_sampled_rows():
         codes = oracle.pack(lin.t)
         ref = oracle.gemm(codes, lin.scale, lin.k, h["x_bits"], threads=THREADS, rows_subset=rows)
         _close(c.y.cpu().numpy()[:, rows], ref[:, rows], c.name)
+
+
+def _item(rng, rows, k, m, swiglu=False, p_zero=synth.P_ZERO, int_x=False):
+    """One batched item with its oracle reference (float64)."""
+    t = synth.ternary(rng, rows, k, p_zero)
+    sc = synth.scales(rng, rows)
+    w, codes = _mat(t, sc)
+    up = upc = su = None
+    if swiglu:
+        tu = synth.ternary(rng, rows, k, p_zero)
+        su = synth.scales(rng, rows)
+        up, upc = _mat(tu, su)
+    xb = synth.small_int_activations(rng, m, k) if int_x else synth.activations(rng, m, k)
+    full, y = _guarded_out(m, rows)
+    if swiglu:
+        ref = oracle.swiglu(codes, sc, upc, su, k, xb, threads=THREADS)
+    else:
+        ref = oracle.gemm(codes, sc, k, xb, threads=THREADS)
+    return (w, up, _dev_x(xb), y, m), ref, full
+
+
+def test_batched_mixed_items():
+    """One batched call over plain GEMVs, SwiGLU pairs and small-M products of
+    several shapes (ragged rows, K spanning several 4096-code chunks, short
+    rows), each element checked against the oracle."""
+    rng = np.random.default_rng(404)
+    specs = [(4096, 4096, 1, False), (1024, 4096, 1, False), (257, 320, 1, False), (640, 4096, 1, True),
+             (300, 12288, 3, False), (4096, 12288, 7, False), (130, 4096, 7, True), (1, 64, 1, False),
+             (33, 192, 8, True), (12288, 4096, 1, True), (200, 8256, 2, False)]
+    made = [_item(rng, r, k, m, sw) for (r, k, m, sw) in specs]
+    tern.tern_gemm_batched([mi[0] for mi in made])
+    torch.cuda.synchronize()
+    assert tern.tern_last_device_error() == tern.TERN_OK
+    for (spec, (it, ref, full)) in zip(specs, made):
+        rows, k, m, sw = spec
+        _close(it[3].cpu().numpy(), ref, f"batched {spec}")
+        _guard_ok(full, m, rows)
+
+
+def test_batched_exact_integers_and_many_items():
+    """More items than one launch carries (split over several launches),
+    integer activations: every result bit-exact."""
+    rng = np.random.default_rng(405)
+    made = [_item(rng, 128 + 64 * (i % 5), 4096 if i % 3 else 12288, 1 + (i % 8), swiglu=(i % 4 == 0), int_x=True)
+            for i in range(60)]
+    tern.tern_gemm_batched([mi[0] for mi in made])
+    torch.cuda.synchronize()
+    for i, (it, ref, full) in enumerate(made):
+        if it[1] is None:
+            assert np.array_equal(it[3].cpu().numpy(), ref.astype(np.float32)), i
+        else:
+            _close(it[3].cpu().numpy(), ref, f"swiglu item {i}")
+
+
+def test_batched_empty_and_degenerate():
+    rng = np.random.default_rng(406)
+    it, ref, full = _item(rng, 100, 256, 2)
+    kzero = tern.TernMatrix(torch.zeros((5, 0), dtype=torch.int32, device="cuda"), torch.ones(5, device="cuda"), 0)
+    y0 = torch.full((1, 5), 3.0, device="cuda")
+    empty = tern.TernMatrix(torch.zeros((0, 4), dtype=torch.int32, device="cuda"), torch.zeros(0, device="cuda"), 64)
+    tern.tern_gemm_batched([])
+    tern.tern_gemm_batched([it, (kzero, None, torch.zeros((1, 8), dtype=torch.bfloat16, device="cuda"), y0, 1),
+                            (empty, None, None, None, 1)])
+    torch.cuda.synchronize()
+    _close(it[3].cpu().numpy(), ref, "batched small")
+    assert not y0.cpu().numpy().any()
+    with pytest.raises(tern.TernError) as e:
+        tern.tern_gemm_batched([(it[0], None, it[2], it[3], 9)])
+    assert e.value.status == tern.TERN_ERR_M_RANGE
