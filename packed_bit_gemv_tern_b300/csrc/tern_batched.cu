@@ -6,19 +6,21 @@
 // Each of the grid's CTAs (one per SM) owns a contiguous run of work units;
 // a unit is one 128-row tile (64 gate + 64 up rows for a SwiGLU pair) of one
 // item over the item's whole K, so no unit needs a cross-CTA reduction.  The
-// host balances the runs by packed bytes.  K is processed in chunks of 4096
+// host balances the runs by packed bytes.  K is processed in chunks of 2048
 // codes; the B operand (activations as two e4m3 terms under a per-row
 // power-of-two scale, see split_pair) and the fp32 accumulators are double
 // buffered per chunk, so staging the next chunk's activations and reading the
 // previous chunk's sums overlap the weight stream.  Roles (17 warps):
 //   * warp 0, lane 0: TMA producer; streams every stage of every unit of the
-//     CTA through a 5-deep ring of 16 KB stages (128 rows x 512 codes,
+//     CTA through a 9-deep ring of 16 KB stages (128 rows x 512 codes,
 //     128-byte swizzle), never waiting on activations.
 //   * warps 1-4: stage B for each chunk (after griddepcontrol.wait), then read
 //     the previous chunk's accumulators, rescale and add them into per-row
 //     registers, and at the end of a unit write y (scale, SiLU gate).
-//   * warps 5-12: two decoder warpgroups taking alternate stages; codes become
-//     e4m3 +-2/0 bytes (decode8) stored to one of three TMEM stage slots.
+//   * warps 5-12: two decoder warpgroups, each decoding half of every stage
+//     (so a stage is ready in half the time and the three TMEM stage slots
+//     leave two stages of slack for the MMAs); codes become e4m3 +-2/0 bytes
+//     (decode8) stored to the stage's TMEM slot.
 //   * warps 13-16, lane 0: MMA issuers; issuer k runs K=32 steps 4k..4k+3 of
 //     every stage (tcgen05.mma kind::f8f6f4, A from TMEM, B from shared
 //     memory, M = 128, N = 16) into its own accumulator of the chunk's buffer.
@@ -50,12 +52,14 @@ constexpr int kStagers = 128;
 constexpr int kFirstDec = 5;               // warps 5-12
 constexpr int kFirstIssuer = 13;           // warps 13-16
 constexpr int kIssuers = 4;
-constexpr int kChunkStages = 8;            // K chunk = 8 stages = 4096 codes
+constexpr int kChunkStages = 4;            // K chunk = 4 stages = 2048 codes
 constexpr int kASlots = 3;                 // TMEM A slots, one stage (128 columns) each
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol = kASlots * 128;  // D[buf][k] at kDCol + 16 * (kIssuers * buf + k)
-constexpr int kBBufBytes = kChunkStages * kStageWords * kBBytesPerWord;  // 64 KB per chunk buffer
-constexpr int kWStages = 5;                // weight ring depth
+constexpr int kBBufBytes = kChunkStages * kStageWords * kBBytesPerWord;  // 32 KB per chunk buffer
+// Weight ring depth: 144 KB in flight per SM, enough to cover DRAM latency at
+// the full HBM rate (a plain TMA stream needs about 128 KB per SM for it).
+constexpr int kWStages = 9;
 
 struct Item {
     const float *scale_g;
@@ -157,14 +161,14 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
     if (tid == 0) {
         for (int s = 0; s < kWStages; ++s) {
             ptx::mbar_init(bars + kBarWFull + 8 * s, 1);
-            ptx::mbar_init(bars + kBarWEmpty + 8 * s, 4);
+            ptx::mbar_init(bars + kBarWEmpty + 8 * s, 8);  // every decoder warp reads every stage
         }
         for (int s = 0; s < kASlots; ++s) {
-            ptx::mbar_init(bars + kBarAFull + 8 * s, 4);
+            ptx::mbar_init(bars + kBarAFull + 8 * s, 8);
             ptx::mbar_init(bars + kBarAEmpty + 8 * s, kIssuers);
         }
         for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(bars + kBarBFull + 8 * b, 4);
+            ptx::mbar_init(bars + kBarBFull + 8 * b, kStagers);  // every staging thread, after its proxy fence
             ptx::mbar_init(bars + kBarBEmpty + 8 * b, kIssuers);
             ptx::mbar_init(bars + kBarDFull + 8 * b, kIssuers);
             ptx::mbar_init(bars + kBarDEmpty + 8 * b, 4);
@@ -227,7 +231,6 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
         bool more = any;
         while (more) {
             for (int st = 0; st < cur.n_stages_chunk && more; ++st, ++gs) {
-                if ((gs & 1) != g) continue;
                 const int wslot = gs % kWStages, aslot = gs % kASlots;
                 uint32_t ok = 1u;
                 if (lane == 0) {
@@ -241,8 +244,9 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                 }
                 ptx::tc_fence_after();
                 const uint32_t srow = row_addr + (uint32_t)wslot * kStageBytes;
-#pragma unroll 1
-                for (int c = 0; c < 4; ++c) {
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {  // warpgroup g takes chunks 2g, 2g+1 of the stage
+                    const int c = 2 * g + cc;
                     const uint4 v0 = ptx::lds128(srow + ((uint32_t)((2 * c) ^ (i & 7)) << 4));
                     const uint4 v1 = ptx::lds128(srow + ((uint32_t)((2 * c + 1) ^ (i & 7)) << 4));
                     uint32_t r[32];
@@ -312,6 +316,9 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
         bool prev_last = false;
         int gc = 0;
         bool ok = any;
+        // what each B buffer holds: a chunk of an item is staged once and reused
+        // by every later tile of the same item that lands on this buffer
+        int held_item[2] = {-1, -1}, held_chunk[2] = {-1, -1}, held_rows[2] = {16, 16};
 
         auto epilogue = [&](int e) {  // read chunk e's accumulators, finish the unit if it was its last chunk
             const int eb = e & 1;
@@ -379,11 +386,22 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
             // the MMAs of chunk gc-2 must be done with this B buffer
             if (gc >= 2 && lane == 0) waiter.wait(bars + kBarBEmpty + 8 * buf, ((gc >> 1) - 1) & 1);
             uint32_t *xm = words + 8 + 8 * buf;
-            if (st_tid < 8) xm[st_tid] = 0u;
+            const bool reuse = held_item[buf] == cur.item && held_chunk[buf] == cur.chunk;
+            if (st_tid < 8 && !reuse) xm[st_tid] = 0u;
             // A failed wait has raised the abort flag before this barrier, so
             // all four staging warps take the same branch after it.
             ptx::named_bar_sync(1, kStagers);
             if (*abort_flag) break;
+            if (reuse) {  // B (and its row scales) already hold this chunk
+                ptx::mbar_arrive(bars + kBarBFull + 8 * buf);
+                if (gc >= 1) epilogue(gc - 1);
+                prev_item = cur.item;
+                prev_tile = cur.tile;
+                prev_last = cur.last_chunk_of_unit();
+                ++gc;
+                ok = cur.next_chunk();
+                continue;
+            }
             const int n_words = cur.n_stages_chunk * kStageWords;
             const int k0 = cur.chunk * kChunkStages * kStageWords * 16;
             const int m = it.m;
@@ -432,15 +450,20 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                     ptx::sts128(at + b_row_off(2 * mm + 1), lo4);
                 }
             }
-            for (int item = st_tid; item < (8 - m) * n_words; item += kStagers) {  // rows n >= 2m are zero
-                const int mm = m + item / n_words, wi = item % n_words;
-                const uint32_t at = bb + (uint32_t)wi * kBBytesPerWord;
-                ptx::sts128(at + b_row_off(2 * mm), make_uint4(0, 0, 0, 0));
-                ptx::sts128(at + b_row_off(2 * mm + 1), make_uint4(0, 0, 0, 0));
+            // Rows n >= 2m must be zero.  Invariant: rows >= held_rows[buf] are
+            // zero over the whole buffer, so only rows [2m, held_rows) are cleared
+            // (over every word, a later chunk may be longer than this one).
+            constexpr int kBufWords = kChunkStages * kStageWords;
+            const int zero_rows = held_rows[buf] - 2 * m;
+            for (int item = st_tid; item < zero_rows * kBufWords; item += kStagers) {
+                const int n = 2 * m + item / kBufWords, wi = item % kBufWords;
+                ptx::sts128(bb + (uint32_t)wi * kBBytesPerWord + b_row_off(n), make_uint4(0, 0, 0, 0));
             }
-            ptx::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(bars + kBarBFull + 8 * buf);
+            held_item[buf] = cur.item;
+            held_chunk[buf] = cur.chunk;
+            held_rows[buf] = 2 * m;
+            ptx::fence_proxy_async_smem();  // my B writes -> visible to the tensor core
+            ptx::mbar_arrive(bars + kBarBFull + 8 * buf);
             if (gc >= 1) epilogue(gc - 1);
             prev_item = cur.item;
             prev_tile = cur.tile;
