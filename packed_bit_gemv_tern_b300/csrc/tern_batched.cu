@@ -10,20 +10,23 @@
 // codes; the B operand (activations as two e4m3 terms under a per-row
 // power-of-two scale, see split_pair) and the fp32 accumulators are double
 // buffered per chunk, so staging the next chunk's activations and reading the
-// previous chunk's sums overlap the weight stream.  Roles (17 warps):
+// previous chunk's sums overlap the weight stream.  A stage splits into four
+// chunk columns of 128 codes per row; column k has its own decoder group, its
+// own MMA issuer and its own TMEM A barriers, so the four columns run as
+// independent pipelines that share only the weight ring and the B and D
+// buffers.  Roles (25 warps):
 //   * warp 0, lane 0: TMA producer; streams every stage of every unit of the
 //     CTA through a 9-deep ring of 16 KB stages (128 rows x 512 codes,
 //     128-byte swizzle), never waiting on activations.
 //   * warps 1-4: stage B for each chunk (after griddepcontrol.wait), then read
 //     the previous chunk's accumulators, rescale and add them into per-row
 //     registers, and at the end of a unit write y (scale, SiLU gate).
-//   * warps 5-12: two decoder warpgroups, each decoding half of every stage
-//     (so a stage is ready in half the time and the three TMEM stage slots
-//     leave two stages of slack for the MMAs); codes become e4m3 +-2/0 bytes
-//     (decode8) stored to the stage's TMEM slot.
-//   * warps 13-16, lane 0: MMA issuers; issuer k runs K=32 steps 4k..4k+3 of
-//     every stage (tcgen05.mma kind::f8f6f4, A from TMEM, B from shared
-//     memory, M = 128, N = 16) into its own accumulator of the chunk's buffer.
+//   * warps 5-20: four decoder groups of four warps; group g turns column g of
+//     each stage into e4m3 +-2/0 bytes (decode8) in the stage's TMEM slot.
+//     Four decoder warps per scheduler hide each other's barrier latency.
+//   * warps 21-24, lane 0: MMA issuers; issuer k runs the K=32 steps of column
+//     k (tcgen05.mma kind::f8f6f4, A from TMEM, B from shared memory,
+//     M = 128, N = 16) into its own accumulator of the chunk's buffer.
 // Every mbarrier wait is bounded; on time-out the kernel records the error,
 // stops, drains its copies and MMAs, releases its tensor memory and returns.
 #include <cuda.h>
@@ -46,12 +49,14 @@ using namespace mma;
 
 constexpr int kMaxItems = 48;              // items per launch (kernel parameter space)
 constexpr int kMaxCtas = 160;
-constexpr int kThreads = 544;              // 17 warps
+constexpr int kThreads = 800;              // 25 warps
 constexpr int kFirstStager = 1;            // warps 1-4
 constexpr int kStagers = 128;
-constexpr int kFirstDec = 5;               // warps 5-12
-constexpr int kFirstIssuer = 13;           // warps 13-16
+constexpr int kFirstDec = 5;               // warps 5-20: decoder group g = chunk column g
+constexpr int kDecWarps = 16;
+constexpr int kFirstIssuer = 21;           // warps 21-24: issuer k = chunk column k
 constexpr int kIssuers = 4;
+constexpr int kCols = 4;                   // chunk columns of a stage (128 codes of a row each)
 constexpr int kChunkStages = 4;            // K chunk = 4 stages = 2048 codes
 constexpr int kASlots = 3;                 // TMEM A slots, one stage (128 columns) each
 constexpr uint32_t kTmemCols = 512;
@@ -88,9 +93,9 @@ constexpr uint32_t kOffXch = kOffB + 2 * kBBufBytes;  // [64][8] fp32
 constexpr uint32_t kOffBar = kOffXch + 64 * 8 * 4;
 constexpr uint32_t kBarWFull = 0;                       // [kWStages]
 constexpr uint32_t kBarWEmpty = kBarWFull + 8 * kWStages;
-constexpr uint32_t kBarAFull = kBarWEmpty + 8 * kWStages;  // [kASlots]
-constexpr uint32_t kBarAEmpty = kBarAFull + 8 * kASlots;
-constexpr uint32_t kBarBFull = kBarAEmpty + 8 * kASlots;   // [2]
+constexpr uint32_t kBarAFull = kBarWEmpty + 8 * kWStages;  // [kASlots][kCols]
+constexpr uint32_t kBarAEmpty = kBarAFull + 8 * kASlots * kCols;
+constexpr uint32_t kBarBFull = kBarAEmpty + 8 * kASlots * kCols;  // [2]
 constexpr uint32_t kBarBEmpty = kBarBFull + 16;
 constexpr uint32_t kBarDFull = kBarBEmpty + 16;
 constexpr uint32_t kBarDEmpty = kBarDFull + 16;
@@ -101,31 +106,32 @@ constexpr uint32_t kSmemBytes = 1024 + kOffBar + kWordsOff + 32 * 4;
 
 __device__ unsigned int g_batched_error;
 
-// Walks the (unit, chunk, stage) sequence of one CTA.
+// Walks the (unit, chunk) sequence of one CTA.  A CTA's units are
+// contiguous, so the item index only moves forward; the fields of the current
+// item live in registers (a dependent search through the parameter space on
+// every unit costs more than a stage of decoding).
 struct Cursor {
     const Params *p;
-    int unit, unit_end, item, tile, chunk, n_chunks, stage_in_chunk, n_stages_chunk;
-    __device__ void set_unit()
+    int unit, unit_end, item, next_unit0, tile, chunk, n_chunks, stages, n_stages_chunk;
+    __device__ void enter_item()
     {
-        item = 0;
-        while (item + 1 < p->n_items && p->item[item + 1].unit0 <= unit) ++item;
-        tile = unit - p->item[item].unit0;
-        chunk = 0;
-        n_chunks = (p->item[item].stages + kChunkStages - 1) / kChunkStages;
-        set_chunk();
+        stages = p->item[item].stages;
+        n_chunks = (stages + kChunkStages - 1) / kChunkStages;
+        next_unit0 = item + 1 < p->n_items ? p->item[item + 1].unit0 : 0x7FFFFFFF;
     }
-    __device__ void set_chunk()
-    {
-        stage_in_chunk = 0;
-        n_stages_chunk = min(kChunkStages, p->item[item].stages - chunk * kChunkStages);
-    }
+    __device__ void set_chunk() { n_stages_chunk = min(kChunkStages, stages - chunk * kChunkStages); }
     __device__ bool begin(const Params *pp, int b)
     {
         p = pp;
         unit = p->unit_start[b];
         unit_end = p->unit_start[b + 1];
         if (unit >= unit_end) return false;
-        set_unit();
+        item = 0;
+        while (item + 1 < p->n_items && p->item[item + 1].unit0 <= unit) ++item;
+        enter_item();
+        tile = unit - p->item[item].unit0;
+        chunk = 0;
+        set_chunk();
         return true;
     }
     // Advance one chunk; false at the end of the CTA's run.
@@ -136,7 +142,14 @@ struct Cursor {
             return true;
         }
         if (++unit >= unit_end) return false;
-        set_unit();
+        chunk = 0;
+        ++tile;
+        if (unit >= next_unit0) {  // every item has at least one unit
+            ++item;
+            enter_item();
+            tile = 0;
+        }
+        set_chunk();
         return true;
     }
     __device__ bool last_chunk_of_unit() const { return chunk + 1 == n_chunks; }
@@ -161,11 +174,11 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
     if (tid == 0) {
         for (int s = 0; s < kWStages; ++s) {
             ptx::mbar_init(bars + kBarWFull + 8 * s, 1);
-            ptx::mbar_init(bars + kBarWEmpty + 8 * s, 8);  // every decoder warp reads every stage
+            ptx::mbar_init(bars + kBarWEmpty + 8 * s, kDecWarps);  // every decoder warp reads every stage
         }
-        for (int s = 0; s < kASlots; ++s) {
-            ptx::mbar_init(bars + kBarAFull + 8 * s, 8);
-            ptx::mbar_init(bars + kBarAEmpty + 8 * s, kIssuers);
+        for (int s = 0; s < kASlots * kCols; ++s) {
+            ptx::mbar_init(bars + kBarAFull + 8 * s, 4);   // the four warps of the column's group
+            ptx::mbar_init(bars + kBarAEmpty + 8 * s, 1);  // the column's issuer
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bars + kBarBFull + 8 * b, kStagers);  // every staging thread, after its proxy fence
@@ -222,51 +235,65 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
         }
     } else if (warp >= kFirstDec && warp < kFirstIssuer) {
         // --------------------------------------------------------- decoders
+        // Group g decodes chunk column g (words 8g..8g+7 of each row) of every
+        // stage into its 32 TMEM columns; quad q owns TMEM lanes 32q..32q+31.
+        // Four decoder warps share each scheduler, so one warp's barrier
+        // round trips hide behind the others' decoding.
         const int g = (warp - kFirstDec) >> 2;
         const int quad = warp & 3;
         const int i = quad * 32 + lane;
         const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
         const uint32_t row_addr = wbuf + (uint32_t)i * 128u;
-        int gs = 0;
+        const uint32_t off0 = (uint32_t)((2 * g) ^ (i & 7)) << 4, off1 = (uint32_t)((2 * g + 1) ^ (i & 7)) << 4;
+        int gs = 0, wslot = 0, aslot = 0;
+        uint32_t wpar = 0, apar = 0;  // phase parities of the current W and A uses
         bool more = any;
         while (more) {
-            for (int st = 0; st < cur.n_stages_chunk && more; ++st, ++gs) {
-                const int wslot = gs % kWStages, aslot = gs % kASlots;
-                uint32_t ok = 1u;
-                if (lane == 0) {
-                    ok = waiter.wait(bars + kBarWFull + 8 * wslot, (gs / kWStages) & 1) ? 1u : 0u;
-                    if (ok && gs >= kASlots)
-                        ok = waiter.wait(bars + kBarAEmpty + 8 * aslot, ((gs / kASlots) - 1) & 1) ? 1u : 0u;
-                }
-                if (__shfl_sync(0xFFFFFFFFu, ok, 0) == 0u) {
+            for (int st = 0; st < cur.n_stages_chunk; ++st) {
+                const uint32_t wf = bars + kBarWFull + 8 * wslot;
+                const uint32_t ae = bars + kBarAEmpty + 8 * (kCols * aslot + g);
+                // both fast-path tests issue back to back; the bounded waits only on a miss
+                bool okw = ptx::mbar_try_wait(wf, wpar);
+                bool oka = gs < kASlots || ptx::mbar_try_wait(ae, apar ^ 1u);
+                if (!okw) okw = waiter.wait(wf, wpar);
+                if (okw && !oka) oka = waiter.wait(ae, apar ^ 1u);
+                if (!__all_sync(0xFFFFFFFFu, okw && oka)) {
                     more = false;
                     break;
                 }
                 ptx::tc_fence_after();
                 const uint32_t srow = row_addr + (uint32_t)wslot * kStageBytes;
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {  // warpgroup g takes chunks 2g, 2g+1 of the stage
-                    const int c = 2 * g + cc;
-                    const uint4 v0 = ptx::lds128(srow + ((uint32_t)((2 * c) ^ (i & 7)) << 4));
-                    const uint4 v1 = ptx::lds128(srow + ((uint32_t)((2 * c + 1) ^ (i & 7)) << 4));
-                    uint32_t r[32];
-                    decode8(v0, v1, r);
-                    ptx::tmem_st_32x32b_x32(tmem + lane_addr + (uint32_t)(aslot * 128 + c * 32), r);
-                }
+                const uint4 v0 = ptx::lds128(srow + off0);
+                const uint4 v1 = ptx::lds128(srow + off1);
+                uint32_t r[32];
+                decode8(v0, v1, r);
+                ptx::tmem_st_32x32b_x32(tmem + lane_addr + (uint32_t)(aslot * 128 + g * 32), r);
                 __syncwarp();
                 if (lane == 0) ptx::mbar_arrive(bars + kBarWEmpty + 8 * wslot);
                 ptx::tmem_wait_st();
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bars + kBarAFull + 8 * aslot);
+                if (lane == 0) ptx::mbar_arrive(bars + kBarAFull + 8 * (kCols * aslot + g));
+                ++gs;
+                if (++wslot == kWStages) {
+                    wslot = 0;
+                    wpar ^= 1u;
+                }
+                if (++aslot == kASlots) {
+                    aslot = 0;
+                    apar ^= 1u;
+                }
             }
             more = more && cur.next_chunk();
         }
     } else if (warp >= kFirstIssuer) {
         // --------------------------------------------------------- MMA issuers
+        // Issuer k runs the K=32 steps of chunk column k (steps 4k..4k+3 of
+        // every stage) into its own accumulator of the chunk's D buffer.
         const int k_iss = warp - kFirstIssuer;
         if (lane == 0 && any) {
-            int gs = 0, gc = 0;
+            int gc = 0, aslot = 0;
+            uint32_t apar = 0;
             bool ok = true;
             while (ok) {
                 const int buf = gc & 1;
@@ -276,22 +303,26 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                 if (!ok) break;
                 ptx::tc_fence_after();
                 const uint32_t bb = bbuf + (uint32_t)buf * kBBufBytes;
-                for (int st = 0; st < cur.n_stages_chunk; ++st, ++gs) {
-                    const int aslot = gs % kASlots;
-                    if (!waiter.wait(bars + kBarAFull + 8 * aslot, (gs / kASlots) & 1)) {
+                for (int st = 0; st < cur.n_stages_chunk; ++st) {
+                    const uint32_t af = bars + kBarAFull + 8 * (kCols * aslot + k_iss);
+                    if (!ptx::mbar_try_wait(af, apar) && !waiter.wait(af, apar)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
-                        const int step = 4 * k_iss + t;           // K=32 step within the stage
+                        const int step = 4 * k_iss + t;              // K=32 step within the stage
                         const int wi = st * kStageWords + 2 * step;  // its first word within the chunk
                         ptx::mma_ts_f8f6f4(d, tmem + (uint32_t)(aslot * 128 + step * 8),
                                            b_desc(bb + (uint32_t)wi * kBBytesPerWord), kIdesc,
                                            (st | t) != 0 ? 1u : 0u);
                     }
-                    ptx::mma_commit(bars + kBarAEmpty + 8 * aslot);
+                    ptx::mma_commit(bars + kBarAEmpty + 8 * (kCols * aslot + k_iss));
+                    if (++aslot == kASlots) {
+                        aslot = 0;
+                        apar ^= 1u;
+                    }
                 }
                 if (!ok) break;
                 ptx::mma_commit(bars + kBarDFull + 8 * buf);
@@ -387,9 +418,10 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
             if (gc >= 2 && lane == 0) waiter.wait(bars + kBarBEmpty + 8 * buf, ((gc >> 1) - 1) & 1);
             uint32_t *xm = words + 8 + 8 * buf;
             const bool reuse = held_item[buf] == cur.item && held_chunk[buf] == cur.chunk;
-            if (st_tid < 8 && !reuse) xm[st_tid] = 0u;
-            // A failed wait has raised the abort flag before this barrier, so
-            // all four staging warps take the same branch after it.
+            // Past this barrier every staging warp has finished chunk gc-2's
+            // epilogue, the last reader of this buffer's row maxima xm.  A
+            // failed wait has raised the abort flag before it, so all four
+            // staging warps take the same branch after it.
             ptx::named_bar_sync(1, kStagers);
             if (*abort_flag) break;
             if (reuse) {  // B (and its row scales) already hold this chunk
@@ -407,7 +439,9 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
             const int m = it.m;
             const int n_items = m * n_words;
             const uint32_t bb = bbuf + (uint32_t)buf * kBBufBytes;
-            constexpr int kBatch = 4;
+            if (st_tid < 8) xm[st_tid] = 0u;
+            ptx::named_bar_sync(1, kStagers);
+            constexpr int kBatch = 2;
             uint4 xa[kBatch], xb[kBatch];
             const bool resident = n_items <= kStagers * kBatch;
             auto load_batch = [&](int first) {

@@ -41,19 +41,20 @@ __device__ __forceinline__ uint64_t b_desc(uint32_t addr)
 struct Waiter {
     volatile uint32_t *abort_flag;  // shared
     unsigned int *err;              // global error word of the kernel
+    // Each try sleeps until the phase completes or kSleepNs pass; the abort
+    // flag and the one-second bound are checked between tries.
+    static constexpr uint32_t kSleepNs = 1000000u;
     __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const
     {
         if (*abort_flag) return false;
+        if (ptx::mbar_try_wait(bar, parity)) return true;
         const long long t0 = clock64();
-        uint32_t spins = 0;
-        while (!ptx::mbar_try_wait(bar, parity)) {
-            if ((++spins & 15u) == 0u) {
-                if (*abort_flag) return false;
-                if (clock64() - t0 > (1ll << 31)) {
-                    atomicOr(err, 1u);
-                    *abort_flag = 1u;
-                    return false;
-                }
+        while (!ptx::mbar_try_wait_sleep(bar, parity, kSleepNs)) {
+            if (*abort_flag) return false;
+            if (clock64() - t0 > (1ll << 31)) {
+                atomicOr(err, 1u);
+                *abort_flag = 1u;
+                return false;
             }
         }
         return true;
@@ -64,7 +65,7 @@ struct Waiter {
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, unsigned int *err)
 {
     const long long t0 = clock64();
-    while (!ptx::mbar_try_wait(bar, parity)) {
+    while (!ptx::mbar_try_wait_sleep(bar, parity, Waiter::kSleepNs)) {
         if (clock64() - t0 > (1ll << 31)) {
             atomicOr(err, 1u);
             return;
