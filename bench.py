@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--rotate-mb", type=int, default=400,
+                    help="c0-c3: MiB of distinct packed weights one step streams (keep above the 126 MB L2)")
     ap.add_argument("--api", default="batched", choices=["batched", "single"],
                     help="batched: one persistent tern_gemm_batched launch per step; single: one launch per call")
     return ap.parse_args()
@@ -303,12 +305,12 @@ def run_ours(args, dist: Dist):
     dev = torch.device("cuda", dist.local)
     torch.cuda.set_device(dev)
     tern.load()
-    wl = workloads.build(args.workload, device=dev, seed_offset=dist.rank)
+    wl = workloads.build(args.workload, device=dev, seed_offset=dist.rank, rotate_bytes=args.rotate_mb * workloads.MiB)
     ncalls = len(wl.calls)
-    launches_per_step = (-(-ncalls // 48)) if args.api == "batched" else ncalls
     stream = torch.cuda.Stream(device=dev)
 
     batch = workloads.batch_of(wl.calls) if args.api == "batched" else None
+    launches_per_step = tern.tern_gemm_batched_launches(batch) if batch is not None else ncalls
 
     def step_fn():
         if batch is not None:
@@ -383,8 +385,8 @@ def run_ours(args, dist: Dist):
                    "algorithmic_bytes_per_step": alg, "us_per_call": round(us_per_call, 4),
                    "l2": "inputs larger than L2: each step streams %.0f MB of distinct buffers" % (packed / 1e6),
                    "graph": "one CUDA graph per step, replayed", "parallelism": f"replicas x{dist.world}",
-                   "api": ("tern_gemm_batched: one persistent launch per 48 calls" if args.api == "batched"
-                           else "one tern_* launch per call")},
+                   "api": (f"tern_gemm_batched: {launches_per_step} persistent launch(es) per step"
+                           if args.api == "batched" else "one tern_* launch per call")},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
@@ -409,23 +411,18 @@ def run_e2e(args, wl, stream, dist: Dist, batch=None):
 
     from packed_bit_gemv_tern_b300 import workloads
 
-    hx = [c.x.cpu().pin_memory() for c in wl.calls]
-    hy = [torch.empty(c.y.shape, dtype=torch.float32).pin_memory() for c in wl.calls]
-    h2d = sum(t.numel() * t.element_size() for t in hx)
-    d2h = sum(t.numel() * t.element_size() for t in hy)
+    hx = wl.x_flat.cpu().pin_memory()
+    hy = torch.empty(wl.y_flat.shape, dtype=torch.float32).pin_memory()
+    h2d = hx.numel() * hx.element_size()
+    d2h = hy.numel() * hy.element_size()
 
     def step():
+        wl.x_flat.copy_(hx, non_blocking=True)
         if batch is not None:
-            for c, x in zip(wl.calls, hx):
-                c.x.copy_(x, non_blocking=True)
             workloads.run_batched(batch, stream)
-            for c, y in zip(wl.calls, hy):
-                y.copy_(c.y, non_blocking=True)
         else:
-            for c, x, y in zip(wl.calls, hx, hy):
-                c.x.copy_(x, non_blocking=True)
-                workloads.run_call(c, stream)
-                y.copy_(c.y, non_blocking=True)
+            workloads.run_calls(wl.calls, stream)
+        hy.copy_(wl.y_flat, non_blocking=True)
         stream.synchronize()
 
     with torch.cuda.stream(stream):
@@ -439,7 +436,8 @@ def run_e2e(args, wl, stream, dist: Dist, batch=None):
     dt = dist.max(dt)
     return {"value": round(dist.world * wl.packed_bytes * args.e2e_steps / dt / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-            "how": "per step: pinned H2D of every x, the tern ABI call(s), D2H of every y; no graph; host-timed"}
+            "how": "per step: one pinned H2D copy of all x, the tern ABI call(s), one D2H copy of all y; "
+                   "no graph; host-timed"}
 
 
 def main():

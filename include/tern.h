@@ -159,9 +159,20 @@ typedef struct {
  * must be independent: no item's y may overlap another item's x, y or
  * weights.  Every item is checked as by the single calls before anything is
  * launched; the first failing item's status is returned and nothing runs.
- * Items are launched in groups of up to 48 in order on `stream`.
- * n == 0 is a no-op; items == NULL gives TERN_ERR_NULL, n < 0 TERN_ERR_SHAPE. */
+ * Items are launched in order on `stream` in groups: one launch takes up to
+ * 112 items holding up to 144 weight matrices (a SwiGLU pair holds two);
+ * an item with k == 0 (y = 0) takes a small launch of its own and one with
+ * rows == 0 none.  n == 0 is a no-op; items == NULL gives TERN_ERR_NULL,
+ * n < 0 TERN_ERR_SHAPE. */
 TERN_API tern_status tern_gemm_batched(const tern_batch_item *items, int32_t n, void *stream);
+
+/* Number of kernel launches tern_gemm_batched makes for these items (host
+ * only, nothing is launched and only items[i].w->rows and ->k are read; the
+ * items are not otherwise checked).  0 for n == 0; a negative tern_status for
+ * n < 0 (-TERN_ERR_SHAPE) or a NULL items array or weight pointer
+ * (-TERN_ERR_NULL).  Not an operation of the model pages: a planning aid for
+ * callers that count or capture launches. */
+TERN_API int32_t tern_gemm_batched_launches(const tern_batch_item *items, int32_t n);
 
 /* Synchronise `stream`, then report and clear the device error word that
  * bounded device-side waits set when they run out (TERN_ERR_TIMEOUT), or a

@@ -36,7 +36,8 @@ TERN_MAX_M = 8
 
 ABI_FUNCTIONS = (
     "tern_pack", "tern_validate", "tern_unpack", "tern_gemv", "tern_gemv_swiglu",
-    "tern_gemm_smallm", "tern_gemm_smallm_swiglu", "tern_gemm_batched", "tern_last_device_error",
+    "tern_gemm_smallm", "tern_gemm_smallm_swiglu", "tern_gemm_batched", "tern_gemm_batched_launches",
+    "tern_last_device_error",
     "tern_status_str", "tern_abi_version",
 )
 
@@ -82,6 +83,7 @@ def load(path: str | None = None):
             "tern_gemm_smallm": [vp, vp, i32, vp, vp],
             "tern_gemm_smallm_swiglu": [vp, vp, vp, i32, vp, vp],
             "tern_gemm_batched": [vp, i32, vp],
+            "tern_gemm_batched_launches": [vp, i32],
             "tern_last_device_error": [vp],
             "tern_status_str": [ctypes.c_int],
             "tern_abi_version": [],
@@ -223,6 +225,15 @@ def tern_gemm_batched(items, stream=None):
     arr = items if isinstance(items, ctypes.Array) else batch_items(items)
     _check(load().tern_gemm_batched(ctypes.cast(arr, ctypes.c_void_p) if len(arr) else None, len(arr),
                                     _stream_handle(stream)), "tern_gemm_batched")
+
+
+def tern_gemm_batched_launches(items) -> int:
+    """Kernel launches tern_gemm_batched makes for these items (host only)."""
+    arr = items if isinstance(items, ctypes.Array) else batch_items(items)
+    n = int(load().tern_gemm_batched_launches(ctypes.cast(arr, ctypes.c_void_p) if len(arr) else None, len(arr)))
+    if n < 0:
+        raise TernError(-n, "tern_gemm_batched_launches")
+    return n
 
 
 def tern_last_device_error(stream=None) -> int:

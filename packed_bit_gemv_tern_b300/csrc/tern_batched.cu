@@ -47,7 +47,8 @@ namespace {
 
 using namespace mma;
 
-constexpr int kMaxItems = 48;              // items per launch (kernel parameter space)
+constexpr int kMaxItems = 112;             // items per launch (kernel parameter space)
+constexpr int kMaxMaps = 144;              // tensor maps per launch: one per item, two per SwiGLU pair
 constexpr int kMaxCtas = 160;
 constexpr int kThreads = 800;              // 25 warps
 constexpr int kFirstStager = 1;            // warps 1-4
@@ -74,6 +75,7 @@ struct Item {
     int rows, k, m, swiglu;
     int stages;  // 512-code stages over K
     int unit0;   // first global unit of this item
+    int map;     // its codes' tensor map (gate, then up, for a SwiGLU pair)
 };
 
 struct Params {
@@ -83,7 +85,7 @@ struct Params {
 };
 
 struct Maps {
-    CUtensorMap m[2 * kMaxItems];  // [2i] plain/gate codes of item i, [2i+1] up codes
+    CUtensorMap m[kMaxMaps];
 };
 
 // Shared-memory layout (bytes from the 1024-aligned base).
@@ -221,12 +223,8 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                     const uint32_t dst = wbuf + slot * kStageBytes, full = bars + kBarWFull + 8 * slot;
                     const int c0 = (cur.chunk * kChunkStages + st) * kStageWords;
                     ptx::mbar_arrive_expect_tx(full, kStageBytes);
-                    if (it.swiglu) {
-                        ptx::tma_load_2d(dst, &maps.m[2 * cur.item], c0, row0, full);
-                        ptx::tma_load_2d(dst + kStageBytes / 2, &maps.m[2 * cur.item + 1], c0, row0, full);
-                    } else {
-                        ptx::tma_load_2d(dst, &maps.m[2 * cur.item], c0, row0, full);
-                    }
+                    ptx::tma_load_2d(dst, &maps.m[it.map], c0, row0, full);
+                    if (it.swiglu) ptx::tma_load_2d(dst + kStageBytes / 2, &maps.m[it.map + 1], c0, row0, full);
                 }
                 more = more && cur.next_chunk();
             }
@@ -518,22 +516,58 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
     }
 }
 
+// End of the group of items that one launch covers, starting at `begin`: up
+// to kMaxItems items with rows > 0 and k > 0, holding up to kMaxMaps tensor
+// maps.  Items with rows == 0 (nothing to do) or k == 0 (y = 0, written by a
+// small CUDA-core launch of their own) ride along without counting.
+int group_end(const tern_batch_item *items, int begin, int n)
+{
+    int cnt = 0, n_maps = 0, idx = begin;
+    for (; idx < n; ++idx) {
+        const tern_batch_item &b = items[idx];
+        if (b.w->rows == 0 || b.w->k == 0) continue;
+        const int need = b.up ? 2 : 1;
+        if (cnt == kMaxItems || n_maps + need > kMaxMaps) break;
+        ++cnt;
+        n_maps += need;
+    }
+    return idx;
+}
+
 }  // namespace
+
+int batched_launches(const tern_batch_item *items, int n)
+{
+    int launches = 0;
+    for (int begin = 0; begin < n;) {
+        const int end = group_end(items, begin, n);
+        bool any = false;
+        for (int i = begin; i < end; ++i) {
+            if (items[i].w->rows == 0) continue;
+            if (items[i].w->k == 0)
+                ++launches;
+            else
+                any = true;
+        }
+        launches += any ? 1 : 0;
+        begin = end;
+    }
+    return launches;
+}
 
 tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t stream)
 {
     static_assert(sizeof(Params) + sizeof(Maps) < 32000, "kernel parameters exceed 32 KB");
     const int sms = sm_count();
     for (int begin = 0; begin < n;) {
-        // one launch covers up to kMaxItems items with rows > 0 and k > 0
+        const int end = group_end(items, begin, n);
         Params prm;
         std::memset(&prm, 0, sizeof(prm));
         Maps maps;
         std::memset(&maps, 0, sizeof(maps));
         std::vector<long long> unit_cost;
-        int cnt = 0, idx = begin;
-        int units = 0;
-        for (; idx < n && cnt < kMaxItems; ++idx) {
+        int cnt = 0, units = 0, n_maps = 0;
+        for (int idx = begin; idx < end; ++idx) {
             const tern_batch_item &b = items[idx];
             if (b.w->rows == 0) continue;
             if (b.w->k == 0) {  // empty sum: y = scale * 0
@@ -552,16 +586,17 @@ tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t strea
             it.swiglu = b.up != nullptr;
             it.stages = (it.k / 16 + kStageWords - 1) / kStageWords;
             it.unit0 = units;
+            it.map = n_maps;
             const int tile_rows = it.swiglu ? 64 : 128;
             const int tiles = (it.rows + tile_rows - 1) / tile_rows;
-            if (!make_code_map(&maps.m[2 * cnt], b.w->codes, it.rows, it.k / 16, tile_rows)) return TERN_ERR_CUDA;
-            if (it.swiglu && !make_code_map(&maps.m[2 * cnt + 1], b.up->codes, it.rows, it.k / 16, tile_rows))
+            if (!make_code_map(&maps.m[n_maps++], b.w->codes, it.rows, it.k / 16, tile_rows)) return TERN_ERR_CUDA;
+            if (it.swiglu && !make_code_map(&maps.m[n_maps++], b.up->codes, it.rows, it.k / 16, tile_rows))
                 return TERN_ERR_CUDA;
             for (int t = 0; t < tiles; ++t) unit_cost.push_back(it.stages);
             units += tiles;
             ++cnt;
         }
-        begin = idx;
+        begin = end;
         if (cnt == 0) continue;
         prm.n_items = cnt;
         // contiguous runs of units with balanced stage counts

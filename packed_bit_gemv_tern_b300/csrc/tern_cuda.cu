@@ -337,6 +337,16 @@ extern "C" tern_status tern_gemm_batched(const tern_batch_item *items, int32_t n
     return batched_dispatch(items, n, (cudaStream_t)stream);
 }
 
+extern "C" int32_t tern_gemm_batched_launches(const tern_batch_item *items, int32_t n)
+{
+    if (n < 0) return -(int32_t)TERN_ERR_SHAPE;
+    if (n == 0) return 0;
+    if (items == nullptr) return -(int32_t)TERN_ERR_NULL;
+    for (int32_t i = 0; i < n; ++i)
+        if (items[i].w == nullptr) return -(int32_t)TERN_ERR_NULL;
+    return batched_launches(items, n);
+}
+
 extern "C" tern_status tern_last_device_error(void *stream)
 {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return TERN_ERR_CUDA;

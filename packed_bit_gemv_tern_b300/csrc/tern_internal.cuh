@@ -24,6 +24,8 @@ tern_status gemm_mma(const tern_matrix *g, const tern_matrix *u, const uint16_t 
 tern_status take_mma_error();
 
 // Persistent batched kernel (tern_batched.cu); items already checked.
+// Number of kernel launches gemm_batched makes for these items (host only).
+int batched_launches(const tern_batch_item *items, int n);
 tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t s);
 tern_status take_batched_error();
 

@@ -92,6 +92,8 @@ class Workload:
         self.calls: list[Call] = []
         self.host = []  # per call: dict(lin=..., up=..., x_bits=...)
         self.distinct = 0
+        self.x_flat = None  # every call's x, contiguous (bf16)
+        self.y_flat = None  # every call's y, contiguous (fp32)
 
     @property
     def packed_bytes(self) -> int:
@@ -192,7 +194,30 @@ def build(name: str, device="cuda", rotate_bytes: int = 400 * MiB, seed_offset: 
         wl.distinct = len(wl.calls)
     else:
         raise ValueError(name)
+    _pack_io(wl, device)
     return wl
+
+
+def _pack_io(wl: Workload, device):
+    """Place every call's x in one bf16 buffer and every y in one fp32 buffer
+    (each call keeps a view), so a step's inputs and outputs move between host
+    and device as one copy each.  Views stay 128-byte aligned: m*k is a
+    multiple of 64 elements."""
+    import torch
+    nx = sum(c.x.numel() for c in wl.calls)
+    ny = sum(c.y.numel() for c in wl.calls)
+    xf = torch.empty(nx, dtype=torch.bfloat16, device=device)
+    yf = torch.zeros(ny, dtype=torch.float32, device=device)
+    ox = oy = 0
+    for c in wl.calls:
+        n = c.x.numel()
+        xf[ox:ox + n].copy_(c.x.reshape(-1))
+        c.x = xf[ox:ox + n].view(c.x.shape)
+        ox += n
+        n = c.y.numel()
+        c.y = yf[oy:oy + n].view(c.y.shape)
+        oy += n
+    wl.x_flat, wl.y_flat = xf, yf
 
 
 def _clone(w: TernMatrix) -> TernMatrix:

@@ -150,3 +150,31 @@ def test_device_entry_points_reject_before_launch(lib):
     assert lib.tern_gemm_smallm(ref(empty), None, 3, None, None) == tern.TERN_OK
     assert lib.tern_gemv_swiglu(ref(empty), ref(empty), None, None, None) == tern.TERN_OK
     assert lib.tern_unpack(ref(empty), None, None) == tern.TERN_OK
+
+
+def test_batched_launch_plan(lib):
+    """Launch count of tern_gemm_batched: 112 items or 144 weight matrices per
+    launch, k == 0 items on a launch of their own, rows == 0 items on none."""
+    keep = []
+
+    def arr(spec):
+        a = (tern.CBatchItem * len(spec))()
+        for i, (rows, k, sw) in enumerate(spec):
+            w = _mat(rows, k)
+            keep.append(w)
+            a[i].w = ctypes.addressof(w)
+            if sw:
+                u = _mat(rows, k)
+                keep.append(u)
+                a[i].up = ctypes.addressof(u)
+            a[i].x, a[i].y, a[i].m = 0x3000, 0x4000, 1
+        return a
+
+    cases = [([(4096, 4096, 0)] * 112, 1), ([(4096, 4096, 0)] * 113, 2), ([(64, 4096, 1)] * 72, 1),
+             ([(64, 4096, 1)] * 73, 2), ([(0, 64, 0)] * 5, 0), ([(4, 0, 0)] * 3, 3),
+             ([(4, 0, 0), (4096, 4096, 0), (0, 4, 0)], 2), ([(4096, 4096, 0)] * 252, 3)]
+    for spec, want in cases:
+        assert tern.tern_gemm_batched_launches(arr(spec)) == want, (len(spec), want)
+    assert lib.tern_gemm_batched_launches(None, 0) == 0
+    assert lib.tern_gemm_batched_launches(None, 3) == -tern.TERN_ERR_NULL
+    assert lib.tern_gemm_batched_launches(None, -1) == -tern.TERN_ERR_SHAPE

@@ -297,7 +297,8 @@ def test_batched_exact_integers_and_many_items():
     integer activations: every result bit-exact."""
     rng = np.random.default_rng(405)
     made = [_item(rng, 128 + 64 * (i % 5), 4096 if i % 3 else 12288, 1 + (i % 8), swiglu=(i % 4 == 0), int_x=True)
-            for i in range(60)]
+            for i in range(150)]
+    assert tern.tern_gemm_batched_launches([mi[0] for mi in made]) == 2
     tern.tern_gemm_batched([mi[0] for mi in made])
     torch.cuda.synchronize()
     for i, (it, ref, full) in enumerate(made):
