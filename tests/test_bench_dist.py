@@ -1,0 +1,58 @@
+"""Multi-rank host logic of bench.py on CPU: two gloo ranks (replicas) meet at
+the barrier and agree on the max-over-ranks time, as the timed region does."""
+import os
+import socket
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket(socket.AF_INET, socket.SOCK_STREAM) as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank), CUDA_VISIBLE_DEVICES="")
+    sys.path.insert(0, ROOT)
+    import bench
+    d = bench.Dist()
+    try:
+        d.barrier()
+        ms = d.max(10.0 * rank + 1.0)   # each rank's own "elapsed time"
+        d.barrier()
+        q.put((d.rank, d.world, ms))
+    finally:
+        d.close()
+
+
+def test_two_gloo_ranks_take_the_max():
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    try:
+        got = sorted(q.get(timeout=120) for _ in procs)
+    finally:
+        for p in procs:
+            p.join(timeout=60)
+    assert got == [(0, 2, 11.0), (1, 2, 11.0)]
+    assert all(p.exitcode == 0 for p in procs)
+
+
+def test_single_rank_needs_no_group():
+    sys.path.insert(0, ROOT)
+    import bench
+    assert bench.reduce_max(None, 3.5) == 3.5
+    d = bench.Dist()
+    assert d.world == int(os.environ.get("WORLD_SIZE", "1"))
+    if d.world == 1:
+        d.barrier()
+        assert d.max(2.0) == 2.0
