@@ -11,19 +11,20 @@
 // power-of-two scale, see split_pair) and the fp32 accumulators are double
 // buffered per chunk, so staging the next chunk's activations and reading the
 // previous chunk's sums overlap the weight stream.  A stage splits into four
-// chunk columns of 128 codes per row; column k has its own decoder group, its
-// own MMA issuer and its own TMEM A barriers, so the four columns run as
-// independent pipelines that share only the weight ring and the B and D
-// buffers.  Roles (25 warps):
+// chunk columns of 128 codes per row, taken in two pairs; each column pair has
+// its own TMEM A barriers and two MMA issuers, and is decoded by one of two
+// decoder groups that alternate stages, so the pairs run as independent
+// pipelines that share only the weight ring and the B and D buffers.  Roles (25 warps):
 //   * warp 0, lane 0: TMA producer; streams every stage of every unit of the
 //     CTA through a 9-deep ring of 16 KB stages (128 rows x 512 codes,
 //     128-byte swizzle), never waiting on activations.
 //   * warps 1-4: stage B for each chunk (after griddepcontrol.wait), then read
 //     the previous chunk's accumulators, rescale and add them into per-row
 //     registers, and at the end of a unit write y (scale, SiLU gate).
-//   * warps 5-20: four decoder groups of four warps; group g turns column g of
-//     each stage into e4m3 +-2/0 bytes (decode8) in the stage's TMEM slot.
-//     Four decoder warps per scheduler hide each other's barrier latency.
+//   * warps 5-20: four decoder groups of four warps; group g turns column
+//     pair g & 1 of the stages of parity g >> 1 into e4m3 +-2/0 bytes
+//     (decode8) in the stage's TMEM slot.  Four decoder warps per scheduler
+//     hide each other's barrier latency.
 //   * warps 21-24, lane 0: MMA issuers; issuer k runs the K=32 steps of column
 //     k (tcgen05.mma kind::f8f6f4, A from TMEM, B from shared memory,
 //     M = 128, N = 16) into its own accumulator of the chunk's buffer.
@@ -53,11 +54,10 @@ constexpr int kMaxCtas = 160;
 constexpr int kThreads = 800;              // 25 warps
 constexpr int kFirstStager = 1;            // warps 1-4
 constexpr int kStagers = 128;
-constexpr int kFirstDec = 5;               // warps 5-20: decoder group g = chunk column g
-constexpr int kDecWarps = 16;
+constexpr int kFirstDec = 5;               // warps 5-20: four decoder groups of four warps
 constexpr int kFirstIssuer = 21;           // warps 21-24: issuer k = chunk column k
 constexpr int kIssuers = 4;
-constexpr int kCols = 4;                   // chunk columns of a stage (128 codes of a row each)
+constexpr int kPairs = 2;                  // column pairs: decoder group g takes pair g & 1 of stages of parity g >> 1
 constexpr int kChunkStages = 4;            // K chunk = 4 stages = 2048 codes
 constexpr int kASlots = 3;                 // TMEM A slots, one stage (128 columns) each
 constexpr uint32_t kTmemCols = 512;
@@ -80,7 +80,9 @@ struct Item {
 
 struct Params {
     int n_items;
+    uint32_t zero;                 // always 0; unknown to the compiler (see the decoders' ring release)
     int unit_start[kMaxCtas + 1];  // CTA b runs units [unit_start[b], unit_start[b + 1])
+    int stages_cta[kMaxCtas];      // 512-code stages in CTA b's run
     Item item[kMaxItems];
 };
 
@@ -95,9 +97,9 @@ constexpr uint32_t kOffXch = kOffB + 2 * kBBufBytes;  // [64][8] fp32
 constexpr uint32_t kOffBar = kOffXch + 64 * 8 * 4;
 constexpr uint32_t kBarWFull = 0;                       // [kWStages]
 constexpr uint32_t kBarWEmpty = kBarWFull + 8 * kWStages;
-constexpr uint32_t kBarAFull = kBarWEmpty + 8 * kWStages;  // [kASlots][kCols]
-constexpr uint32_t kBarAEmpty = kBarAFull + 8 * kASlots * kCols;
-constexpr uint32_t kBarBFull = kBarAEmpty + 8 * kASlots * kCols;  // [2]
+constexpr uint32_t kBarAFull = kBarWEmpty + 8 * kWStages;  // [kASlots][kPairs]
+constexpr uint32_t kBarAEmpty = kBarAFull + 8 * kASlots * kPairs;
+constexpr uint32_t kBarBFull = kBarAEmpty + 8 * kASlots * kPairs;  // [2]
 constexpr uint32_t kBarBEmpty = kBarBFull + 16;
 constexpr uint32_t kBarDFull = kBarBEmpty + 16;
 constexpr uint32_t kBarDEmpty = kBarDFull + 16;
@@ -176,11 +178,11 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
     if (tid == 0) {
         for (int s = 0; s < kWStages; ++s) {
             ptx::mbar_init(bars + kBarWFull + 8 * s, 1);
-            ptx::mbar_init(bars + kBarWEmpty + 8 * s, kDecWarps);  // every decoder warp reads every stage
+            ptx::mbar_init(bars + kBarWEmpty + 8 * s, 8 * 32);  // every lane of the stage's two decoder groups
         }
-        for (int s = 0; s < kASlots * kCols; ++s) {
-            ptx::mbar_init(bars + kBarAFull + 8 * s, 4);   // the four warps of the column's group
-            ptx::mbar_init(bars + kBarAEmpty + 8 * s, 1);  // the column's issuer
+        for (int s = 0; s < kASlots * kPairs; ++s) {
+            ptx::mbar_init(bars + kBarAFull + 8 * s, 4 * 32);  // every lane of the decoding group
+            ptx::mbar_init(bars + kBarAEmpty + 8 * s, 2);      // the pair's two issuers
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bars + kBarBFull + 8 * b, kStagers);  // every staging thread, after its proxy fence
@@ -208,15 +210,19 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
 
     if (warp == 0) {
         // --------------------------------------------------------- producer
+        // "Empty" barriers are waited at the flipped parity: a fresh barrier
+        // counts its preceding phase as complete, so the first pass through
+        // the ring needs no special case.
         if (lane == 0 && any) {
-            int gs = 0;
+            int gs = 0, slot = 0;
+            uint32_t par = 0;
             bool more = true;
             while (more) {
                 const Item &it = p.item[cur.item];
                 const int row0 = cur.tile * (it.swiglu ? 64 : 128);
                 for (int st = 0; st < cur.n_stages_chunk; ++st, ++gs) {
-                    const int slot = gs % kWStages;
-                    if (gs >= kWStages && !waiter.wait(bars + kBarWEmpty + 8 * slot, ((gs / kWStages) - 1) & 1)) {
+                    const uint32_t empty = bars + kBarWEmpty + 8 * slot;
+                    if (!ptx::mbar_try_wait(empty, par ^ 1u) && !waiter.wait(empty, par ^ 1u)) {
                         more = false;
                         break;
                     }
@@ -225,6 +231,10 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                     ptx::mbar_arrive_expect_tx(full, kStageBytes);
                     ptx::tma_load_2d(dst, &maps.m[it.map], c0, row0, full);
                     if (it.swiglu) ptx::tma_load_2d(dst + kStageBytes / 2, &maps.m[it.map + 1], c0, row0, full);
+                    if (++slot == kWStages) {
+                        slot = 0;
+                        par ^= 1u;
+                    }
                 }
                 more = more && cur.next_chunk();
             }
@@ -233,90 +243,110 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
         }
     } else if (warp >= kFirstDec && warp < kFirstIssuer) {
         // --------------------------------------------------------- decoders
-        // Group g decodes chunk column g (words 8g..8g+7 of each row) of every
-        // stage into its 32 TMEM columns; quad q owns TMEM lanes 32q..32q+31.
-        // Four decoder warps share each scheduler, so one warp's barrier
-        // round trips hide behind the others' decoding.
+        // Group g decodes column pair cp = g & 1 (columns 2cp and 2cp+1: words
+        // 16cp..16cp+15 of each row) of the stages of parity g >> 1 into the
+        // stage's TMEM slot; quad q owns TMEM lanes 32q..32q+31.  Four decoder
+        // warps share each scheduler, so one warp's barrier round trips hide
+        // behind the others' decoding.  Every lane arrives on the barriers (no
+        // divergent single-lane branch per stage).
         const int g = (warp - kFirstDec) >> 2;
+        const int cp = g & 1, sp = g >> 1;
         const int quad = warp & 3;
         const int i = quad * 32 + lane;
-        const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
+        const uint32_t tm_row = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(cp * 64);
         const uint32_t row_addr = wbuf + (uint32_t)i * 128u;
-        const uint32_t off0 = (uint32_t)((2 * g) ^ (i & 7)) << 4, off1 = (uint32_t)((2 * g + 1) ^ (i & 7)) << 4;
-        int gs = 0, wslot = 0, aslot = 0;
-        uint32_t wpar = 0, apar = 0;  // phase parities of the current W and A uses
-        bool more = any;
-        while (more) {
-            for (int st = 0; st < cur.n_stages_chunk; ++st) {
-                const uint32_t wf = bars + kBarWFull + 8 * wslot;
-                const uint32_t ae = bars + kBarAEmpty + 8 * (kCols * aslot + g);
-                // both fast-path tests issue back to back; the bounded waits only on a miss
-                bool okw = ptx::mbar_try_wait(wf, wpar);
-                bool oka = gs < kASlots || ptx::mbar_try_wait(ae, apar ^ 1u);
-                if (!okw) okw = waiter.wait(wf, wpar);
-                if (okw && !oka) oka = waiter.wait(ae, apar ^ 1u);
-                if (!__all_sync(0xFFFFFFFFu, okw && oka)) {
-                    more = false;
-                    break;
-                }
-                ptx::tc_fence_after();
-                const uint32_t srow = row_addr + (uint32_t)wslot * kStageBytes;
-                const uint4 v0 = ptx::lds128(srow + off0);
-                const uint4 v1 = ptx::lds128(srow + off1);
+        // 16-byte chunks 4cp..4cp+3 of the row, under the 128-byte swizzle
+        const uint32_t o0 = (uint32_t)((4 * cp + 0) ^ (i & 7)) << 4, o1 = (uint32_t)((4 * cp + 1) ^ (i & 7)) << 4;
+        const uint32_t o2 = (uint32_t)((4 * cp + 2) ^ (i & 7)) << 4, o3 = (uint32_t)((4 * cp + 3) ^ (i & 7)) << 4;
+        const int total = any ? p.stages_cta[blockIdx.x] : 0;
+        const uint32_t zero = p.zero;
+        int wslot = sp, aslot = sp;   // stage s = sp: ring slot s % kWStages, TMEM slot s % kASlots
+        uint32_t wpar = 0, apar = 0;  // phase parities of those uses
+        for (int s = sp; s < total; s += 2) {
+            const uint32_t wf = bars + kBarWFull + 8 * wslot;
+            const uint32_t ae = bars + kBarAEmpty + 8 * (kPairs * aslot + cp);
+            // The weights move to registers and the ring slot is released before
+            // waiting for the TMEM slot, so refills never wait on MMAs.  The
+            // release must not overtake the loads: its barrier address is made
+            // to depend on one word of each 128-bit load (a vector load
+            // completes as a whole), through a zero the compiler cannot see,
+            // so the arrive issues only once every load has returned.
+            bool okw = ptx::mbar_try_wait(wf, wpar);
+            if (!okw) okw = waiter.wait(wf, wpar);
+            if (!__all_sync(0xFFFFFFFFu, okw)) break;
+            const uint32_t srow = row_addr + (uint32_t)wslot * kStageBytes;
+            const uint4 v0 = ptx::lds128(srow + o0), v1 = ptx::lds128(srow + o1);
+            const uint4 v2 = ptx::lds128(srow + o2), v3 = ptx::lds128(srow + o3);
+            const uint32_t dep = v0.x ^ v1.x ^ v2.x ^ v3.x;
+            ptx::mbar_arrive(bars + kBarWEmpty + 8 * wslot + (dep & zero));
+            bool oka = ptx::mbar_try_wait(ae, apar ^ 1u);
+            if (!oka) oka = waiter.wait(ae, apar ^ 1u);
+            if (!__all_sync(0xFFFFFFFFu, oka)) break;
+            ptx::tc_fence_after();
+            const uint32_t ta = tm_row + (uint32_t)(aslot * 128);
+            {
                 uint32_t r[32];
                 decode8(v0, v1, r);
-                ptx::tmem_st_32x32b_x32(tmem + lane_addr + (uint32_t)(aslot * 128 + g * 32), r);
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bars + kBarWEmpty + 8 * wslot);
-                ptx::tmem_wait_st();
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bars + kBarAFull + 8 * (kCols * aslot + g));
-                ++gs;
-                if (++wslot == kWStages) {
-                    wslot = 0;
-                    wpar ^= 1u;
-                }
-                if (++aslot == kASlots) {
-                    aslot = 0;
-                    apar ^= 1u;
-                }
+                ptx::tmem_st_32x32b_x32(ta, r);
             }
-            more = more && cur.next_chunk();
+            {
+                uint32_t r[32];
+                decode8(v2, v3, r);
+                ptx::tmem_st_32x32b_x32(ta + 32u, r);
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bars + kBarAFull + 8 * (kPairs * aslot + cp));
+            wslot += 2;
+            if (wslot >= kWStages) {
+                wslot -= kWStages;
+                wpar ^= 1u;
+            }
+            aslot += 2;
+            if (aslot >= kASlots) {
+                aslot -= kASlots;
+                apar ^= 1u;
+            }
         }
     } else if (warp >= kFirstIssuer) {
         // --------------------------------------------------------- MMA issuers
         // Issuer k runs the K=32 steps of chunk column k (steps 4k..4k+3 of
-        // every stage) into its own accumulator of the chunk's D buffer.
+        // every stage) into its own accumulator of the chunk's D buffer.  The
+        // B descriptor is formed once per chunk and advanced by adding the
+        // operand offset to its start-address field (addresses stay below
+        // 256 KB, so the 14-bit field never carries).
         const int k_iss = warp - kFirstIssuer;
+        const int cp = k_iss >> 1;
         if (lane == 0 && any) {
             int gc = 0, aslot = 0;
             uint32_t apar = 0;
             bool ok = true;
+            const uint32_t a_col = tmem + (uint32_t)(k_iss * 32);
             while (ok) {
                 const int buf = gc & 1;
                 const uint32_t d = tmem + kDCol + 16u * (uint32_t)(kIssuers * buf + k_iss);
-                ok = waiter.wait(bars + kBarBFull + 8 * buf, (gc >> 1) & 1);
-                if (ok && gc >= 2) ok = waiter.wait(bars + kBarDEmpty + 8 * buf, ((gc >> 1) - 1) & 1);
+                const uint32_t bfull = bars + kBarBFull + 8 * buf, dempty = bars + kBarDEmpty + 8 * buf;
+                const uint32_t bpar = (uint32_t)(gc >> 1) & 1u;
+                ok = (ptx::mbar_try_wait(bfull, bpar) || waiter.wait(bfull, bpar)) &&
+                     (ptx::mbar_try_wait(dempty, bpar ^ 1u) || waiter.wait(dempty, bpar ^ 1u));
                 if (!ok) break;
                 ptx::tc_fence_after();
-                const uint32_t bb = bbuf + (uint32_t)buf * kBBufBytes;
+                // column k's first word in the chunk buffer: word 8k of stage 0
+                const uint64_t bd0 = b_desc(bbuf + (uint32_t)buf * kBBufBytes + (uint32_t)(8 * k_iss) * kBBytesPerWord);
                 for (int st = 0; st < cur.n_stages_chunk; ++st) {
-                    const uint32_t af = bars + kBarAFull + 8 * (kCols * aslot + k_iss);
+                    const uint32_t af = bars + kBarAFull + 8 * (kPairs * aslot + cp);
                     if (!ptx::mbar_try_wait(af, apar) && !waiter.wait(af, apar)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
+                    const uint64_t bd = bd0 + (uint64_t)((st * kStageWords * kBBytesPerWord) >> 4);
+                    const uint32_t a = a_col + (uint32_t)(aslot * 128);
 #pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const int step = 4 * k_iss + t;              // K=32 step within the stage
-                        const int wi = st * kStageWords + 2 * step;  // its first word within the chunk
-                        ptx::mma_ts_f8f6f4(d, tmem + (uint32_t)(aslot * 128 + step * 8),
-                                           b_desc(bb + (uint32_t)wi * kBBytesPerWord), kIdesc,
+                    for (int t = 0; t < 4; ++t)  // K=32 step 4k+t: A columns +8t, B words +2t
+                        ptx::mma_ts_f8f6f4(d, a + 8u * t, bd + (uint64_t)((2 * t * kBBytesPerWord) >> 4), kIdesc,
                                            (st | t) != 0 ? 1u : 0u);
-                    }
-                    ptx::mma_commit(bars + kBarAEmpty + 8 * (kCols * aslot + k_iss));
+                    ptx::mma_commit(bars + kBarAEmpty + 8 * (kPairs * aslot + cp));
                     if (++aslot == kASlots) {
                         aslot = 0;
                         apar ^= 1u;
@@ -413,7 +443,7 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
             const int buf = gc & 1;
             const Item &it = p.item[cur.item];
             // the MMAs of chunk gc-2 must be done with this B buffer
-            if (gc >= 2 && lane == 0) waiter.wait(bars + kBarBEmpty + 8 * buf, ((gc >> 1) - 1) & 1);
+            if (lane == 0) waiter.wait(bars + kBarBEmpty + 8 * buf, ((gc >> 1) & 1) ^ 1);
             uint32_t *xm = words + 8 + 8 * buf;
             const bool reuse = held_item[buf] == cur.item && held_chunk[buf] == cur.chunk;
             // Past this barrier every staging warp has finished chunk gc-2's
@@ -599,6 +629,7 @@ tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t strea
         begin = end;
         if (cnt == 0) continue;
         prm.n_items = cnt;
+        prm.zero = 0u;
         // contiguous runs of units with balanced stage counts
         const int ctas = units < sms ? units : (sms < kMaxCtas ? sms : kMaxCtas);
         long long total = 0;
@@ -612,6 +643,11 @@ tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t strea
             prm.unit_start[b] = u;
         }
         prm.unit_start[ctas] = units;
+        for (int b = 0; b < ctas; ++b) {
+            long long st = 0;
+            for (int q = prm.unit_start[b]; q < prm.unit_start[b + 1]; ++q) st += unit_cost[q];
+            prm.stages_cta[b] = (int)st;
+        }
 
         if (cudaFuncSetAttribute(k_tern_batched, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
             cudaSuccess)
