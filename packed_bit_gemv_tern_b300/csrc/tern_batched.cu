@@ -312,8 +312,12 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
         // --------------------------------------------------------- MMA issuers
         // Issuer k runs the K=32 steps of chunk column k (steps 4k..4k+3 of
         // every stage) into its own accumulator of the chunk's D buffer.  The
-        // B descriptor is formed once per chunk and advanced by adding the
-        // operand offset to its start-address field (addresses stay below
+        // issuing thread shares its scheduler with four busy decoder warps,
+        // so its per-stage path is kept to the barrier test, the fence, the
+        // four MMAs and the commit: the chunk's stage loop is unrolled, and
+        // slots, parities, barrier addresses and descriptor offsets are
+        // formed from the chunk start.  The B descriptor's start-address
+        // field is advanced by adding operand offsets (addresses stay below
         // 256 KB, so the 14-bit field never carries).
         const int k_iss = warp - kFirstIssuer;
         const int cp = k_iss >> 1;
@@ -322,6 +326,8 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
             uint32_t apar = 0;
             bool ok = true;
             const uint32_t a_col = tmem + (uint32_t)(k_iss * 32);
+            const uint32_t af0 = bars + kBarAFull + 8u * (uint32_t)cp;   // slot a: + 8 * kPairs * a
+            const uint32_t ae0 = bars + kBarAEmpty + 8u * (uint32_t)cp;
             while (ok) {
                 const int buf = gc & 1;
                 const uint32_t d = tmem + kDCol + 16u * (uint32_t)(kIssuers * buf + k_iss);
@@ -333,24 +339,26 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                 ptx::tc_fence_after();
                 // column k's first word in the chunk buffer: word 8k of stage 0
                 const uint64_t bd0 = b_desc(bbuf + (uint32_t)buf * kBBufBytes + (uint32_t)(8 * k_iss) * kBBytesPerWord);
-                for (int st = 0; st < cur.n_stages_chunk; ++st) {
-                    const uint32_t af = bars + kBarAFull + 8 * (kPairs * aslot + cp);
+                const int n_st = cur.n_stages_chunk;
+#pragma unroll
+                for (int st = 0; st < kChunkStages; ++st) {
+                    if (st >= n_st) break;
+                    const uint32_t af = af0 + (uint32_t)(8 * kPairs * aslot);
                     if (!ptx::mbar_try_wait(af, apar) && !waiter.wait(af, apar)) {
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint64_t bd = bd0 + (uint64_t)((st * kStageWords * kBBytesPerWord) >> 4);
                     const uint32_t a = a_col + (uint32_t)(aslot * 128);
+                    const uint64_t bd = bd0 + (uint64_t)((st * kStageWords * kBBytesPerWord) >> 4);
 #pragma unroll
                     for (int t = 0; t < 4; ++t)  // K=32 step 4k+t: A columns +8t, B words +2t
                         ptx::mma_ts_f8f6f4(d, a + 8u * t, bd + (uint64_t)((2 * t * kBBytesPerWord) >> 4), kIdesc,
                                            (st | t) != 0 ? 1u : 0u);
-                    ptx::mma_commit(bars + kBarAEmpty + 8 * (kPairs * aslot + cp));
-                    if (++aslot == kASlots) {
-                        aslot = 0;
-                        apar ^= 1u;
-                    }
+                    ptx::mma_commit(ae0 + (uint32_t)(8 * kPairs * aslot));
+                    const bool wrap = aslot == kASlots - 1;
+                    aslot = wrap ? 0 : aslot + 1;
+                    apar ^= wrap ? 1u : 0u;
                 }
                 if (!ok) break;
                 ptx::mma_commit(bars + kBarDFull + 8 * buf);
