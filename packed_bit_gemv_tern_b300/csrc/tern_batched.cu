@@ -6,10 +6,12 @@
 // Each of the grid's CTAs (one per SM) owns a contiguous run of work units;
 // a unit is one 128-row tile (64 gate + 64 up rows for a SwiGLU pair) of one
 // item over the item's whole K, so no unit needs a cross-CTA reduction.  The
-// host balances the runs by packed bytes.  K is processed in chunks of 2048
-// codes; the B operand (activations as two e4m3 terms under a per-row
-// power-of-two scale, see split_pair) and the fp32 accumulators are double
-// buffered per chunk, so staging the next chunk's activations and reading the
+// host balances the runs by packed bytes.  K is processed in chunks of up to
+// 16384 / m codes (the whole K for m = 1 at every Neutrino shape); the B
+// operand (activations as two e4m3 terms under a per-row power-of-two scale,
+// see split_pair) and the fp32 accumulators are double buffered per chunk, a
+// chunk's B is reused by every later tile of the item on the same buffer, and
+// staging the next chunk's activations and reading the
 // previous chunk's sums overlap the weight stream.  A stage splits into four
 // chunk columns of 128 codes per row, taken in two pairs; each column pair has
 // its own TMEM A barriers and two MMA issuers, and is decoded by one of two
@@ -58,11 +60,17 @@ constexpr int kFirstDec = 5;               // warps 5-20: four decoder groups of
 constexpr int kFirstIssuer = 21;           // warps 21-24: issuer k = chunk column k
 constexpr int kIssuers = 4;
 constexpr int kPairs = 2;                  // column pairs: decoder group g takes pair g & 1 of stages of parity g >> 1
-constexpr int kChunkStages = 4;            // K chunk = 4 stages = 2048 codes
+constexpr int kMaxChunkStages = 32;        // a K chunk is up to 32 stages (16384 codes), 32 / m stages
 constexpr int kASlots = 3;                 // TMEM A slots, one stage (128 columns) each
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol = kASlots * 128;  // D[buf][k] at kDCol + 16 * (kIssuers * buf + k)
-constexpr int kBBufBytes = kChunkStages * kStageWords * kBBytesPerWord;  // 32 KB per chunk buffer
+// B buffer of one chunk in the compact layout: the 2m rows (hi/lo of each
+// activation row) of a 16-code block are contiguous, blocks 32m bytes apart.
+// The MMA reads eight rows of a core matrix from each block start and eight
+// more 128 bytes on, so rows past 2m (ignored D columns) read neighbouring
+// blocks' bytes and the last block reads up to 256 bytes past its start.
+constexpr int kBBufBytes = 32768;
+constexpr int kBBufStride = kBBufBytes + 256;
 // Weight ring depth: 144 KB in flight per SM, enough to cover DRAM latency at
 // the full HBM rate (a plain TMA stream needs about 128 KB per SM for it).
 constexpr int kWStages = 9;
@@ -74,6 +82,7 @@ struct Item {
     float *y;
     int rows, k, m, swiglu;
     int stages;  // 512-code stages over K
+    int cstages; // stages per K chunk: min(stages, 32 / m), so a chunk's B fits one buffer
     int unit0;   // first global unit of this item
     int map;     // its codes' tensor map (gate, then up, for a SwiGLU pair)
 };
@@ -93,7 +102,7 @@ struct Maps {
 // Shared-memory layout (bytes from the 1024-aligned base).
 constexpr uint32_t kOffW = 0;
 constexpr uint32_t kOffB = kOffW + kWStages * kStageBytes;
-constexpr uint32_t kOffXch = kOffB + 2 * kBBufBytes;  // [64][8] fp32
+constexpr uint32_t kOffXch = kOffB + 2 * kBBufStride;  // [64][8] fp32
 constexpr uint32_t kOffBar = kOffXch + 64 * 8 * 4;
 constexpr uint32_t kBarWFull = 0;                       // [kWStages]
 constexpr uint32_t kBarWEmpty = kBarWFull + 8 * kWStages;
@@ -116,14 +125,15 @@ __device__ unsigned int g_batched_error;
 // every unit costs more than a stage of decoding).
 struct Cursor {
     const Params *p;
-    int unit, unit_end, item, next_unit0, tile, chunk, n_chunks, stages, n_stages_chunk;
+    int unit, unit_end, item, next_unit0, tile, chunk, n_chunks, stages, cstages, n_stages_chunk;
     __device__ void enter_item()
     {
         stages = p->item[item].stages;
-        n_chunks = (stages + kChunkStages - 1) / kChunkStages;
+        cstages = p->item[item].cstages;
+        n_chunks = (stages + cstages - 1) / cstages;
         next_unit0 = item + 1 < p->n_items ? p->item[item + 1].unit0 : 0x7FFFFFFF;
     }
-    __device__ void set_chunk() { n_stages_chunk = min(kChunkStages, stages - chunk * kChunkStages); }
+    __device__ void set_chunk() { n_stages_chunk = min(cstages, stages - chunk * cstages); }
     __device__ bool begin(const Params *pp, int b)
     {
         p = pp;
@@ -227,7 +237,7 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                         break;
                     }
                     const uint32_t dst = wbuf + slot * kStageBytes, full = bars + kBarWFull + 8 * slot;
-                    const int c0 = (cur.chunk * kChunkStages + st) * kStageWords;
+                    const int c0 = (cur.chunk * cur.cstages + st) * kStageWords;
                     ptx::mbar_arrive_expect_tx(full, kStageBytes);
                     ptx::tma_load_2d(dst, &maps.m[it.map], c0, row0, full);
                     if (it.swiglu) ptx::tma_load_2d(dst + kStageBytes / 2, &maps.m[it.map + 1], c0, row0, full);
@@ -337,12 +347,13 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                      (ptx::mbar_try_wait(dempty, bpar ^ 1u) || waiter.wait(dempty, bpar ^ 1u));
                 if (!ok) break;
                 ptx::tc_fence_after();
-                // column k's first word in the chunk buffer: word 8k of stage 0
-                const uint64_t bd0 = b_desc(bbuf + (uint32_t)buf * kBBufBytes + (uint32_t)(8 * k_iss) * kBBytesPerWord);
+                // compact B: 16-code blocks 32m bytes apart; column k starts at word 8k
+                const uint32_t wbytes = 32u * (uint32_t)p.item[cur.item].m;
+                const uint64_t bd0 = b_desc_lbo(bbuf + (uint32_t)buf * kBBufStride + (uint32_t)(8 * k_iss) * wbytes, wbytes);
+                const uint32_t st_step = (kStageWords * wbytes) >> 4, t_step = (2u * wbytes) >> 4;
                 const int n_st = cur.n_stages_chunk;
-#pragma unroll
-                for (int st = 0; st < kChunkStages; ++st) {
-                    if (st >= n_st) break;
+                uint64_t bd = bd0;
+                for (int st = 0; st < n_st; ++st, bd += st_step) {
                     const uint32_t af = af0 + (uint32_t)(8 * kPairs * aslot);
                     if (!ptx::mbar_try_wait(af, apar) && !waiter.wait(af, apar)) {
                         ok = false;
@@ -350,11 +361,10 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                     }
                     ptx::tc_fence_after();
                     const uint32_t a = a_col + (uint32_t)(aslot * 128);
-                    const uint64_t bd = bd0 + (uint64_t)((st * kStageWords * kBBytesPerWord) >> 4);
+                    ptx::mma_ts_f8f6f4(d, a, bd, kIdesc, st != 0 ? 1u : 0u);
 #pragma unroll
-                    for (int t = 0; t < 4; ++t)  // K=32 step 4k+t: A columns +8t, B words +2t
-                        ptx::mma_ts_f8f6f4(d, a + 8u * t, bd + (uint64_t)((2 * t * kBBytesPerWord) >> 4), kIdesc,
-                                           (st | t) != 0 ? 1u : 0u);
+                    for (int t = 1; t < 4; ++t)  // K=32 step 4k+t: A columns +8t, B words +2t
+                        ptx::mma_ts_f8f6f4(d, a + 8u * t, bd + (uint64_t)(t_step * t), kIdesc, 1u);
                     ptx::mma_commit(ae0 + (uint32_t)(8 * kPairs * aslot));
                     const bool wrap = aslot == kASlots - 1;
                     aslot = wrap ? 0 : aslot + 1;
@@ -385,7 +395,7 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
         bool ok = any;
         // what each B buffer holds: a chunk of an item is staged once and reused
         // by every later tile of the same item that lands on this buffer
-        int held_item[2] = {-1, -1}, held_chunk[2] = {-1, -1}, held_rows[2] = {16, 16};
+        int held_item[2] = {-1, -1}, held_chunk[2] = {-1, -1};
 
         auto epilogue = [&](int e) {  // read chunk e's accumulators, finish the unit if it was its last chunk
             const int eb = e & 1;
@@ -471,10 +481,11 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                 continue;
             }
             const int n_words = cur.n_stages_chunk * kStageWords;
-            const int k0 = cur.chunk * kChunkStages * kStageWords * 16;
+            const int k0 = cur.chunk * cur.cstages * kStageWords * 16;
             const int m = it.m;
             const int n_items = m * n_words;
-            const uint32_t bb = bbuf + (uint32_t)buf * kBBufBytes;
+            const uint32_t bb = bbuf + (uint32_t)buf * kBBufStride;
+            const uint32_t wbytes = 32u * (uint32_t)m;  // compact B: a block holds rows 0..2m-1
             if (st_tid < 8) xm[st_tid] = 0u;
             ptx::named_bar_sync(1, kStagers);
             constexpr int kBatch = 2;
@@ -515,23 +526,13 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                     const int mm = item / n_words, wi = item - mm * n_words;
                     uint4 hi4 = make_uint4(0, 0, 0, 0), lo4 = make_uint4(0, 0, 0, 0);
                     if (k0 + 16 * wi < it.k) split_word(xa[t], xb[t], exp2i(row_scale_exp(xm[mm])), hi4, lo4);
-                    const uint32_t at = bb + (uint32_t)wi * kBBytesPerWord;
-                    ptx::sts128(at + b_row_off(2 * mm), hi4);
-                    ptx::sts128(at + b_row_off(2 * mm + 1), lo4);
+                    const uint32_t at = bb + (uint32_t)wi * wbytes + 32u * (uint32_t)mm;
+                    ptx::sts128(at, hi4);
+                    ptx::sts128(at + 16u, lo4);
                 }
-            }
-            // Rows n >= 2m must be zero.  Invariant: rows >= held_rows[buf] are
-            // zero over the whole buffer, so only rows [2m, held_rows) are cleared
-            // (over every word, a later chunk may be longer than this one).
-            constexpr int kBufWords = kChunkStages * kStageWords;
-            const int zero_rows = held_rows[buf] - 2 * m;
-            for (int item = st_tid; item < zero_rows * kBufWords; item += kStagers) {
-                const int n = 2 * m + item / kBufWords, wi = item % kBufWords;
-                ptx::sts128(bb + (uint32_t)wi * kBBytesPerWord + b_row_off(n), make_uint4(0, 0, 0, 0));
             }
             held_item[buf] = cur.item;
             held_chunk[buf] = cur.chunk;
-            held_rows[buf] = 2 * m;
             ptx::fence_proxy_async_smem();  // my B writes -> visible to the tensor core
             ptx::mbar_arrive(bars + kBarBFull + 8 * buf);
             if (gc >= 1) epilogue(gc - 1);
@@ -623,6 +624,7 @@ tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t strea
             it.m = b.m;
             it.swiglu = b.up != nullptr;
             it.stages = (it.k / 16 + kStageWords - 1) / kStageWords;
+            it.cstages = it.stages < kMaxChunkStages / it.m ? it.stages : kMaxChunkStages / it.m;
             it.unit0 = units;
             it.map = n_maps;
             const int tile_rows = it.swiglu ? 64 : 128;

@@ -35,6 +35,14 @@ __device__ __forceinline__ uint64_t b_desc(uint32_t addr)
            (1ull << 46);
 }
 
+// Descriptor of a K-major, unswizzled B operand whose 16-code blocks sit
+// `lbo` bytes apart (rows 0-7 of a block at +0, rows 8-15 at +128).
+__device__ __forceinline__ uint64_t b_desc_lbo(uint32_t addr, uint32_t lbo)
+{
+    return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)(128u >> 4) << 32) | (1ull << 46);
+}
+
 // Spin on an mbarrier phase with a time bound (~1 s).  On time-out the
 // kernel's error word and the CTA's abort flag are set; once the abort flag is
 // up every later wait returns false at once.
