@@ -60,7 +60,6 @@ constexpr int kFirstDec = 5;               // warps 5-20: four decoder groups of
 constexpr int kFirstIssuer = 21;           // warps 21-24: issuer k = chunk column k
 constexpr int kIssuers = 4;
 constexpr int kPairs = 2;                  // column pairs: decoder group g takes pair g & 1 of stages of parity g >> 1
-constexpr int kMaxChunkStages = 32;        // a K chunk is up to 32 stages (16384 codes), 32 / m stages
 constexpr int kASlots = 3;                 // TMEM A slots, one stage (128 columns) each
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol = kASlots * 128;  // D[buf][k] at kDCol + 16 * (kIssuers * buf + k)
@@ -69,11 +68,18 @@ constexpr uint32_t kDCol = kASlots * 128;  // D[buf][k] at kDCol + 16 * (kIssuer
 // The MMA reads eight rows of a core matrix from each block start and eight
 // more 128 bytes on, so rows past 2m (ignored D columns) read neighbouring
 // blocks' bytes and the last block reads up to 256 bytes past its start.
-constexpr int kBBufBytes = 32768;
+#ifndef TERN_BBUF_KB
+#define TERN_BBUF_KB 48
+#endif
+constexpr int kBBufBytes = TERN_BBUF_KB * 1024;
 constexpr int kBBufStride = kBBufBytes + 256;
-// Weight ring depth: 144 KB in flight per SM, enough to cover DRAM latency at
-// the full HBM rate (a plain TMA stream needs about 128 KB per SM for it).
-constexpr int kWStages = 9;
+// Weight ring depth: 112 KB in flight per SM covers DRAM latency at the HBM
+// rate (a plain TMA stream of these stages runs as fast with 6 as with 9);
+// the rest of shared memory goes to the two 48 KB activation buffers.
+#ifndef TERN_WSTAGES
+#define TERN_WSTAGES 7
+#endif
+constexpr int kWStages = TERN_WSTAGES;
 
 struct Item {
     const float *scale_g;
@@ -488,48 +494,37 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
             const uint32_t wbytes = 32u * (uint32_t)m;  // compact B: a block holds rows 0..2m-1
             if (st_tid < 8) xm[st_tid] = 0u;
             ptx::named_bar_sync(1, kStagers);
-            constexpr int kBatch = 2;
-            uint4 xa[kBatch], xb[kBatch];
-            const bool resident = n_items <= kStagers * kBatch;
-            auto load_batch = [&](int first) {
-#pragma unroll
-                for (int t = 0; t < kBatch; ++t) {
-                    const int item = first + t * kStagers;
-                    xa[t] = make_uint4(0, 0, 0, 0);
-                    xb[t] = make_uint4(0, 0, 0, 0);
-                    if (item < n_items) {
-                        const int mm = item / n_words, wi = item - mm * n_words;
-                        const int kk = k0 + 16 * wi;
-                        if (kk < it.k) {
-                            const uint4 *src = reinterpret_cast<const uint4 *>(it.x + (size_t)mm * it.k + kk);
-                            xa[t] = src[0];
-                            xb[t] = src[1];
-                        }
-                    }
-                }
-            };
-            for (int first = st_tid; first < n_items; first += kStagers * kBatch) {
-                load_batch(first);
-#pragma unroll
-                for (int t = 0; t < kBatch; ++t) {
-                    const int item = first + t * kStagers;
-                    if (item < n_items) atomicMax(&xm[item / n_words], max_abs16(xa[t], xb[t]));
-                }
+            // The compact layout keeps 32 bytes (hi and lo rows) per 16
+            // activations of a row, the size of the 16 bf16 values, so each
+            // word is copied asynchronously to its final place (all copies in
+            // flight at once, zero-filled past K), its row maximum reduced
+            // from shared memory, and split in place.  A warp's 32 items are
+            // 32 consecutive words of one activation row (n_words is a
+            // multiple of 32), so the maximum is reduced in the warp first.
+            for (int item = st_tid; item < n_items; item += kStagers) {
+                const int mm = item / n_words, wi = item - mm * n_words;
+                const int kk = k0 + 16 * wi;
+                const bool in_k = kk < it.k;
+                const uint16_t *src = in_k ? it.x + (size_t)mm * it.k + kk : it.x;
+                const uint32_t at = bb + (uint32_t)wi * wbytes + 32u * (uint32_t)mm;
+                ptx::cp_async16(at, src, in_k ? 16u : 0u);
+                ptx::cp_async16(at + 16u, src + 8, in_k ? 16u : 0u);
+            }
+            ptx::cp_async_wait_all();
+            for (int item = st_tid; item < n_items; item += kStagers) {
+                const int mm = item / n_words, wi = item - mm * n_words;
+                const uint32_t at = bb + (uint32_t)wi * wbytes + 32u * (uint32_t)mm;
+                const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, max_abs16(ptx::lds128(at), ptx::lds128(at + 16u)));
+                if (lane == 0) atomicMax(&xm[mm], mx);
             }
             ptx::named_bar_sync(1, kStagers);
-            for (int first = st_tid; first < n_items; first += kStagers * kBatch) {
-                if (!resident) load_batch(first);
-#pragma unroll
-                for (int t = 0; t < kBatch; ++t) {
-                    const int item = first + t * kStagers;
-                    if (item >= n_items) break;
-                    const int mm = item / n_words, wi = item - mm * n_words;
-                    uint4 hi4 = make_uint4(0, 0, 0, 0), lo4 = make_uint4(0, 0, 0, 0);
-                    if (k0 + 16 * wi < it.k) split_word(xa[t], xb[t], exp2i(row_scale_exp(xm[mm])), hi4, lo4);
-                    const uint32_t at = bb + (uint32_t)wi * wbytes + 32u * (uint32_t)mm;
-                    ptx::sts128(at, hi4);
-                    ptx::sts128(at + 16u, lo4);
-                }
+            for (int item = st_tid; item < n_items; item += kStagers) {
+                const int mm = item / n_words, wi = item - mm * n_words;
+                const uint32_t at = bb + (uint32_t)wi * wbytes + 32u * (uint32_t)mm;
+                uint4 hi4, lo4;
+                split_word(ptx::lds128(at), ptx::lds128(at + 16u), exp2i(row_scale_exp(xm[mm])), hi4, lo4);
+                ptx::sts128(at, hi4);
+                ptx::sts128(at + 16u, lo4);
             }
             held_item[buf] = cur.item;
             held_chunk[buf] = cur.chunk;
@@ -624,7 +619,8 @@ tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t strea
             it.m = b.m;
             it.swiglu = b.up != nullptr;
             it.stages = (it.k / 16 + kStageWords - 1) / kStageWords;
-            it.cstages = it.stages < kMaxChunkStages / it.m ? it.stages : kMaxChunkStages / it.m;
+            const int cap = kBBufBytes / (1024 * it.m);  // stages of compact B one buffer holds
+            it.cstages = it.stages < cap ? it.stages : cap;
             it.unit0 = units;
             it.map = n_maps;
             const int tile_rows = it.swiglu ? 64 : 128;

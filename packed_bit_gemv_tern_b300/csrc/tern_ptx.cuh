@@ -213,6 +213,19 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr)
     return v;
 }
 
+// 16-byte asynchronous global -> shared copy (L2 only); `bytes` < 16 fills
+// the rest of the destination with zeros (0 reads nothing).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, uint32_t bytes)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(bytes) : "memory");
+}
+
+// Wait until every cp.async this thread issued has landed.
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v)
 {
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
