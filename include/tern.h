@@ -159,10 +159,13 @@ typedef struct {
  * must be independent: no item's y may overlap another item's x, y or
  * weights.  Every item is checked as by the single calls before anything is
  * launched; the first failing item's status is returned and nothing runs.
- * Items are launched in order on `stream` in groups: one launch takes up to
- * 112 items holding up to 144 weight matrices (a SwiGLU pair holds two);
- * an item with k == 0 (y = 0) takes a small launch of its own and one with
- * rows == 0 none.  n == 0 is a no-op; items == NULL gives TERN_ERR_NULL,
+ * Items are launched in order on `stream` in groups of consecutive items:
+ * a launch takes up to 128 items holding up to 144 weight matrices (a SwiGLU
+ * pair holds two), and a batch that needs several launches is spread evenly
+ * over the fewest that fit; an item with k == 0 (y = 0) takes a small launch
+ * of its own and one with rows == 0 none.  Tensor maps of the weights are
+ * encoded once per (codes, shape) and cached by the library, so repeated
+ * calls on resident weights cost a lookup on the host.  n == 0 is a no-op; items == NULL gives TERN_ERR_NULL,
  * n < 0 TERN_ERR_SHAPE. */
 TERN_API tern_status tern_gemm_batched(const tern_batch_item *items, int32_t n, void *stream);
 

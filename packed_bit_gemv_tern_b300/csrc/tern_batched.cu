@@ -50,7 +50,7 @@ namespace {
 
 using namespace mma;
 
-constexpr int kMaxItems = 112;             // items per launch (kernel parameter space)
+constexpr int kMaxItems = 128;             // items per launch (kernel parameter space)
 constexpr int kMaxMaps = 144;              // tensor maps per launch: one per item, two per SwiGLU pair
 constexpr int kMaxCtas = 160;
 constexpr int kThreads = 800;              // 25 warps
@@ -550,31 +550,49 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
     }
 }
 
-// End of the group of items that one launch covers, starting at `begin`: up
-// to kMaxItems items with rows > 0 and k > 0, holding up to kMaxMaps tensor
-// maps.  Items with rows == 0 (nothing to do) or k == 0 (y = 0, written by a
-// small CUDA-core launch of their own) ride along without counting.
-int group_end(const tern_batch_item *items, int begin, int n)
+// Launch groups of a batch: consecutive runs of items, each with up to
+// kMaxItems items that have rows > 0 and k > 0 ("real" items) holding up to
+// kMaxMaps tensor maps.  The fewest groups a greedy walk needs is found
+// first, then the real items are spread evenly over that many groups (a
+// short last launch streams far below the rate of a full one).  Items with
+// rows == 0 (nothing to do) or k == 0 (y = 0, written by a small CUDA-core
+// launch of their own) ride along without counting.  Returns the end index of
+// each group.
+std::vector<int> plan_groups(const tern_batch_item *items, int n)
 {
-    int cnt = 0, n_maps = 0, idx = begin;
-    for (; idx < n; ++idx) {
-        const tern_batch_item &b = items[idx];
-        if (b.w->rows == 0 || b.w->k == 0) continue;
-        const int need = b.up ? 2 : 1;
-        if (cnt == kMaxItems || n_maps + need > kMaxMaps) break;
-        ++cnt;
-        n_maps += need;
-    }
-    return idx;
+    auto walk = [&](int per_group) {
+        std::vector<int> ends;
+        int cnt = 0, n_maps = 0;
+        for (int idx = 0; idx < n; ++idx) {
+            const tern_batch_item &b = items[idx];
+            if (b.w->rows == 0 || b.w->k == 0) continue;
+            const int need = b.up ? 2 : 1;
+            if (cnt == per_group || n_maps + need > kMaxMaps) {
+                ends.push_back(idx);
+                cnt = 0;
+                n_maps = 0;
+            }
+            ++cnt;
+            n_maps += need;
+        }
+        ends.push_back(n);
+        return ends;
+    };
+    int real = 0;
+    for (int idx = 0; idx < n; ++idx) real += (items[idx].w->rows != 0 && items[idx].w->k != 0) ? 1 : 0;
+    const std::vector<int> greedy = walk(kMaxItems);
+    if (greedy.size() <= 1) return greedy;
+    const int per = (real + (int)greedy.size() - 1) / (int)greedy.size();
+    std::vector<int> even = walk(per);
+    return even.size() <= greedy.size() ? even : greedy;
 }
 
 }  // namespace
 
 int batched_launches(const tern_batch_item *items, int n)
 {
-    int launches = 0;
-    for (int begin = 0; begin < n;) {
-        const int end = group_end(items, begin, n);
+    int launches = 0, begin = 0;
+    for (const int end : plan_groups(items, n)) {
         bool any = false;
         for (int i = begin; i < end; ++i) {
             if (items[i].w->rows == 0) continue;
@@ -593,8 +611,18 @@ tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t strea
 {
     static_assert(sizeof(Params) + sizeof(Maps) < 32000, "kernel parameters exceed 32 KB");
     const int sms = sm_count();
-    for (int begin = 0; begin < n;) {
-        const int end = group_end(items, begin, n);
+    // the kernel's shared-memory attribute, once per device
+    static bool attr_set[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TERN_ERR_CUDA;
+    if (!attr_set[dev]) {
+        if (cudaFuncSetAttribute(k_tern_batched, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+            cudaSuccess)
+            return TERN_ERR_CUDA;
+        attr_set[dev] = true;
+    }
+    int begin = 0;
+    for (const int end : plan_groups(items, n)) {
         Params prm;
         std::memset(&prm, 0, sizeof(prm));
         Maps maps;
@@ -655,9 +683,6 @@ tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t strea
             prm.stages_cta[b] = (int)st;
         }
 
-        if (cudaFuncSetAttribute(k_tern_batched, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-            cudaSuccess)
-            return TERN_ERR_CUDA;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)ctas, 1, 1);
         cfg.blockDim = dim3(kThreads, 1, 1);

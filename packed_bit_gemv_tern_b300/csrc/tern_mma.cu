@@ -49,6 +49,9 @@
 
 #include <cstdint>
 #include <cstring>
+#include <functional>
+#include <mutex>
+#include <unordered_map>
 
 #include "tern.h"
 #include "tern_internal.cuh"
@@ -528,17 +531,59 @@ static EncodeTiled encode_fn()
     return fn;
 }
 
+namespace {
+
+// Encoded tensor maps by (codes, rows, kw, box_rows): a map depends on
+// nothing else, so a reused key (the same matrix called again, or a new
+// allocation at the same address with the same shape) reuses its map and the
+// per-call host cost of a batch of resident weights is a table lookup.
+struct MapKey {
+    const uint32_t *codes;
+    int rows, kw, box_rows;
+    bool operator==(const MapKey &o) const
+    {
+        return codes == o.codes && rows == o.rows && kw == o.kw && box_rows == o.box_rows;
+    }
+};
+struct MapKeyHash {
+    size_t operator()(const MapKey &k) const
+    {
+        size_t h = std::hash<const void *>()(k.codes);
+        h ^= ((size_t)k.rows * 0x9E3779B97F4A7C15ull) + ((size_t)k.kw << 20) + (size_t)k.box_rows;
+        return h;
+    }
+};
+constexpr size_t kMapCacheMax = 8192;
+std::mutex g_map_mu;
+std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_map_cache;
+
+}  // namespace
+
 bool make_code_map(CUtensorMap *m, const uint32_t *codes, int rows, int kw, int box_rows)
 {
+    const MapKey key{codes, rows, kw, box_rows};
+    {
+        std::lock_guard<std::mutex> lk(g_map_mu);
+        auto f = g_map_cache.find(key);
+        if (f != g_map_cache.end()) {
+            *m = f->second;
+            return true;
+        }
+    }
     EncodeTiled fn = encode_fn();
     if (fn == nullptr) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)kw, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)kw * 4};
     const cuuint32_t box[2] = {(cuuint32_t)kStageWords, (cuuint32_t)box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t *>(codes), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    if (fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 2, const_cast<uint32_t *>(codes), dims, strides, box, estr,
+           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    if (g_map_cache.size() >= kMapCacheMax) g_map_cache.clear();
+    g_map_cache.emplace(key, *m);
+    return true;
 }
 
 }  // namespace mma

@@ -153,7 +153,7 @@ def test_device_entry_points_reject_before_launch(lib):
 
 
 def test_batched_launch_plan(lib):
-    """Launch count of tern_gemm_batched: 112 items or 144 weight matrices per
+    """Launch count of tern_gemm_batched: 128 items or 144 weight matrices per
     launch, k == 0 items on a launch of their own, rows == 0 items on none."""
     keep = []
 
@@ -170,9 +170,10 @@ def test_batched_launch_plan(lib):
             a[i].x, a[i].y, a[i].m = 0x3000, 0x4000, 1
         return a
 
-    cases = [([(4096, 4096, 0)] * 112, 1), ([(4096, 4096, 0)] * 113, 2), ([(64, 4096, 1)] * 72, 1),
+    cases = [([(4096, 4096, 0)] * 128, 1), ([(4096, 4096, 0)] * 129, 2), ([(64, 4096, 1)] * 72, 1),
              ([(64, 4096, 1)] * 73, 2), ([(0, 64, 0)] * 5, 0), ([(4, 0, 0)] * 3, 3),
-             ([(4, 0, 0), (4096, 4096, 0), (0, 4, 0)], 2), ([(4096, 4096, 0)] * 252, 3)]
+             ([(4, 0, 0), (4096, 4096, 0), (0, 4, 0)], 2), ([(4096, 4096, 0)] * 252, 2),
+             ([(4096, 4096, 0)] * 257, 3), ([(4096, 4096, 0)] * 100 + [(64, 4096, 1)] * 30, 2)]
     for spec, want in cases:
         assert tern.tern_gemm_batched_launches(arr(spec)) == want, (len(spec), want)
     assert lib.tern_gemm_batched_launches(None, 0) == 0
