@@ -12,22 +12,18 @@
 // see split_pair) and the fp32 accumulators are double buffered per chunk, a
 // chunk's B is reused by every later tile of the item on the same buffer, and
 // staging the next chunk's activations and reading the
-// previous chunk's sums overlap the weight stream.  A stage splits into four
-// chunk columns of 128 codes per row, taken in two pairs; each column pair has
-// its own TMEM A barriers and two MMA issuers, and is decoded by one of two
-// decoder groups that alternate stages, so the pairs run as independent
-// pipelines that share only the weight ring and the B and D buffers.  Roles (25 warps):
+// previous chunk's sums overlap the weight stream.  Roles (21 warps):
 //   * warp 0, lane 0: TMA producer; streams every stage of every unit of the
-//     CTA through a 9-deep ring of 16 KB stages (128 rows x 512 codes,
+//     CTA through a 6-deep ring of 16 KB stages (128 rows x 512 codes,
 //     128-byte swizzle), never waiting on activations.
 //   * warps 1-4: stage B for each chunk (after griddepcontrol.wait), then read
 //     the previous chunk's accumulators, rescale and add them into per-row
 //     registers, and at the end of a unit write y (scale, SiLU gate).
-//   * warps 5-20: four decoder groups of four warps; group g turns column
-//     pair g & 1 of the stages of parity g >> 1 into e4m3 +-2/0 bytes
-//     (decode8) in the stage's TMEM slot.  Four decoder warps per scheduler
-//     hide each other's barrier latency.
-//   * warps 21-24, lane 0: MMA issuers; issuer k runs the K=32 steps of column
+//   * warps 5-16: three decoder groups of four warps; group g turns the four
+//     chunk columns (128 codes of a row each) of the stages s = g (mod 3)
+//     into e4m3 +-2/0 bytes (decode8) in TMEM slot g.  Three decoder warps
+//     per scheduler hide each other's barrier latency.
+//   * warps 17-20, lane 0: MMA issuers; issuer k runs the K=32 steps of column
 //     k (tcgen05.mma kind::f8f6f4, A from TMEM, B from shared memory,
 //     M = 128, N = 16) into its own accumulator of the chunk's buffer.
 // Every mbarrier wait is bounded; on time-out the kernel records the error,
@@ -53,13 +49,17 @@ using namespace mma;
 constexpr int kMaxItems = 128;             // items per launch (kernel parameter space)
 constexpr int kMaxMaps = 144;              // tensor maps per launch: one per item, two per SwiGLU pair
 constexpr int kMaxCtas = 160;
-constexpr int kThreads = 800;              // 25 warps
+constexpr int kThreads = 672;              // 21 warps
 constexpr int kFirstStager = 1;            // warps 1-4
 constexpr int kStagers = 128;
-constexpr int kFirstDec = 5;               // warps 5-20: four decoder groups of four warps
-constexpr int kFirstIssuer = 21;           // warps 21-24: issuer k = chunk column k
+constexpr int kFirstDec = 5;               // warps 5-16: three decoder groups of four warps
+constexpr int kFirstIssuer = 17;           // warps 17-20: issuer k = chunk column k
 constexpr int kIssuers = 4;
-constexpr int kPairs = 2;                  // column pairs: decoder group g takes pair g & 1 of stages of parity g >> 1
+// Decoder group g decodes the stages s = g (mod 3) into TMEM slot g and ring
+// slots g and g + 3: every slot a group waits on was last used by the group
+// itself, so a phase-parity wait can never be two phases ahead (which would
+// alias).
+constexpr int kDecGroups = 3;
 constexpr int kASlots = 3;                 // TMEM A slots, one stage (128 columns) each
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kDCol = kASlots * 128;  // D[buf][k] at kDCol + 16 * (kIssuers * buf + k)
@@ -69,15 +69,16 @@ constexpr uint32_t kDCol = kASlots * 128;  // D[buf][k] at kDCol + 16 * (kIssuer
 // more 128 bytes on, so rows past 2m (ignored D columns) read neighbouring
 // blocks' bytes and the last block reads up to 256 bytes past its start.
 #ifndef TERN_BBUF_KB
-#define TERN_BBUF_KB 48
+#define TERN_BBUF_KB 56
 #endif
 constexpr int kBBufBytes = TERN_BBUF_KB * 1024;
 constexpr int kBBufStride = kBBufBytes + 256;
-// Weight ring depth: 112 KB in flight per SM covers DRAM latency at the HBM
+// Weight ring depth: 96 KB in flight per SM covers DRAM latency at the HBM
 // rate (a plain TMA stream of these stages runs as fast with 6 as with 9);
-// the rest of shared memory goes to the two 48 KB activation buffers.
+// the rest of shared memory goes to the two 56 KB activation buffers.  The
+// depth is a multiple of kDecGroups (see there).
 #ifndef TERN_WSTAGES
-#define TERN_WSTAGES 7
+#define TERN_WSTAGES 6
 #endif
 constexpr int kWStages = TERN_WSTAGES;
 
@@ -95,7 +96,6 @@ struct Item {
 
 struct Params {
     int n_items;
-    uint32_t zero;                 // always 0; unknown to the compiler (see the decoders' ring release)
     int unit_start[kMaxCtas + 1];  // CTA b runs units [unit_start[b], unit_start[b + 1])
     int stages_cta[kMaxCtas];      // 512-code stages in CTA b's run
     Item item[kMaxItems];
@@ -112,9 +112,9 @@ constexpr uint32_t kOffXch = kOffB + 2 * kBBufStride;  // [64][8] fp32
 constexpr uint32_t kOffBar = kOffXch + 64 * 8 * 4;
 constexpr uint32_t kBarWFull = 0;                       // [kWStages]
 constexpr uint32_t kBarWEmpty = kBarWFull + 8 * kWStages;
-constexpr uint32_t kBarAFull = kBarWEmpty + 8 * kWStages;  // [kASlots][kPairs]
-constexpr uint32_t kBarAEmpty = kBarAFull + 8 * kASlots * kPairs;
-constexpr uint32_t kBarBFull = kBarAEmpty + 8 * kASlots * kPairs;  // [2]
+constexpr uint32_t kBarAFull = kBarWEmpty + 8 * kWStages;  // [kASlots]
+constexpr uint32_t kBarAEmpty = kBarAFull + 8 * kASlots;
+constexpr uint32_t kBarBFull = kBarAEmpty + 8 * kASlots;    // [2]
 constexpr uint32_t kBarBEmpty = kBarBFull + 16;
 constexpr uint32_t kBarDFull = kBarBEmpty + 16;
 constexpr uint32_t kBarDEmpty = kBarDFull + 16;
@@ -194,11 +194,11 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
     if (tid == 0) {
         for (int s = 0; s < kWStages; ++s) {
             ptx::mbar_init(bars + kBarWFull + 8 * s, 1);
-            ptx::mbar_init(bars + kBarWEmpty + 8 * s, 8 * 32);  // every lane of the stage's two decoder groups
+            ptx::mbar_init(bars + kBarWEmpty + 8 * s, 4 * 32);  // every lane of the stage's decoder group
         }
-        for (int s = 0; s < kASlots * kPairs; ++s) {
+        for (int s = 0; s < kASlots; ++s) {
             ptx::mbar_init(bars + kBarAFull + 8 * s, 4 * 32);  // every lane of the decoding group
-            ptx::mbar_init(bars + kBarAEmpty + 8 * s, 2);      // the pair's two issuers
+            ptx::mbar_init(bars + kBarAEmpty + 8 * s, kIssuers);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bars + kBarBFull + 8 * b, kStagers);  // every staging thread, after its proxy fence
@@ -259,70 +259,55 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
         }
     } else if (warp >= kFirstDec && warp < kFirstIssuer) {
         // --------------------------------------------------------- decoders
-        // Group g decodes column pair cp = g & 1 (columns 2cp and 2cp+1: words
-        // 16cp..16cp+15 of each row) of the stages of parity g >> 1 into the
-        // stage's TMEM slot; quad q owns TMEM lanes 32q..32q+31.  Four decoder
+        // Group g decodes all four columns of the stages s = g (mod 3) into
+        // TMEM slot g; quad q owns TMEM lanes 32q..32q+31.  Three decoder
         // warps share each scheduler, so one warp's barrier round trips hide
-        // behind the others' decoding.  Every lane arrives on the barriers (no
-        // divergent single-lane branch per stage).
+        // behind the others' decoding, and a warp's control work is paid once
+        // per stage it decodes.  Every lane arrives on the
+        // barriers (no divergent single-lane path).  The ring slot is released
+        // after the last TMEM store, which consumes the last loaded words.
         const int g = (warp - kFirstDec) >> 2;
-        const int cp = g & 1, sp = g >> 1;
         const int quad = warp & 3;
         const int i = quad * 32 + lane;
-        const uint32_t tm_row = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(cp * 64);
+        const uint32_t tm_row = tmem + ((uint32_t)(quad * 32) << 16);
         const uint32_t row_addr = wbuf + (uint32_t)i * 128u;
-        // 16-byte chunks 4cp..4cp+3 of the row, under the 128-byte swizzle
-        const uint32_t o0 = (uint32_t)((4 * cp + 0) ^ (i & 7)) << 4, o1 = (uint32_t)((4 * cp + 1) ^ (i & 7)) << 4;
-        const uint32_t o2 = (uint32_t)((4 * cp + 2) ^ (i & 7)) << 4, o3 = (uint32_t)((4 * cp + 3) ^ (i & 7)) << 4;
+        const uint32_t sw = (uint32_t)(i & 7);  // 128-byte swizzle: 16-byte chunk c of row i sits at c ^ (i & 7)
         const int total = any ? p.stages_cta[blockIdx.x] : 0;
-        const uint32_t zero = p.zero;
-        int wslot = sp, aslot = sp;   // stage s = sp: ring slot s % kWStages, TMEM slot s % kASlots
-        uint32_t wpar = 0, apar = 0;  // phase parities of those uses
-        for (int s = sp; s < total; s += 2) {
-            const uint32_t wf = bars + kBarWFull + 8 * wslot;
-            const uint32_t ae = bars + kBarAEmpty + 8 * (kPairs * aslot + cp);
-            // The weights move to registers and the ring slot is released before
-            // waiting for the TMEM slot, so refills never wait on MMAs.  The
-            // release must not overtake the loads: its barrier address is made
-            // to depend on one word of each 128-bit load (a vector load
-            // completes as a whole), through a zero the compiler cannot see,
-            // so the arrive issues only once every load has returned.
+        static_assert(kWStages % kDecGroups == 0 && kASlots == kDecGroups, "slots must cycle within a group");
+        int w_r = g, w_q = 0;  // stage s: ring slot s % kWStages, use s / kWStages
+        int a_q = 0;           //          TMEM slot g = s % kASlots, use s / kASlots
+        const int a_r = g;
+        for (int s = g; s < total; s += kDecGroups) {
+            const uint32_t wf = bars + kBarWFull + 8 * w_r;
+            const uint32_t ae = bars + kBarAEmpty + 8 * a_r;
+            const uint32_t wpar = (uint32_t)w_q & 1u, apar = (uint32_t)a_q & 1u;
+            // both fast-path tests issue back to back; the bounded waits only on a miss
             bool okw = ptx::mbar_try_wait(wf, wpar);
-            if (!okw) okw = waiter.wait(wf, wpar);
-            if (!__all_sync(0xFFFFFFFFu, okw)) break;
-            const uint32_t srow = row_addr + (uint32_t)wslot * kStageBytes;
-            const uint4 v0 = ptx::lds128(srow + o0), v1 = ptx::lds128(srow + o1);
-            const uint4 v2 = ptx::lds128(srow + o2), v3 = ptx::lds128(srow + o3);
-            const uint32_t dep = v0.x ^ v1.x ^ v2.x ^ v3.x;
-            ptx::mbar_arrive(bars + kBarWEmpty + 8 * wslot + (dep & zero));
             bool oka = ptx::mbar_try_wait(ae, apar ^ 1u);
-            if (!oka) oka = waiter.wait(ae, apar ^ 1u);
-            if (!__all_sync(0xFFFFFFFFu, oka)) break;
+            if (!okw) okw = waiter.wait(wf, wpar);
+            if (okw && !oka) oka = waiter.wait(ae, apar ^ 1u);
+            if (!__all_sync(0xFFFFFFFFu, okw && oka)) break;
             ptx::tc_fence_after();
-            const uint32_t ta = tm_row + (uint32_t)(aslot * 128);
-            {
+            const uint32_t srow = row_addr + (uint32_t)w_r * kStageBytes;
+            const uint32_t ta = tm_row + (uint32_t)(a_r * 128);
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+                const uint4 v0 = ptx::lds128(srow + ((((uint32_t)(2 * c)) ^ sw) << 4));
+                const uint4 v1 = ptx::lds128(srow + ((((uint32_t)(2 * c + 1)) ^ sw) << 4));
                 uint32_t r[32];
                 decode8(v0, v1, r);
-                ptx::tmem_st_32x32b_x32(ta, r);
+                ptx::tmem_st_32x32b_x32(ta + 32u * (uint32_t)c, r);
             }
-            {
-                uint32_t r[32];
-                decode8(v2, v3, r);
-                ptx::tmem_st_32x32b_x32(ta + 32u, r);
-            }
+            ptx::mbar_arrive(bars + kBarWEmpty + 8 * w_r);
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bars + kBarAFull + 8 * (kPairs * aslot + cp));
-            wslot += 2;
-            if (wslot >= kWStages) {
-                wslot -= kWStages;
-                wpar ^= 1u;
+            ptx::mbar_arrive(bars + kBarAFull + 8 * a_r);
+            w_r += kDecGroups;  // s += 3
+            if (w_r >= kWStages) {
+                w_r -= kWStages;
+                ++w_q;
             }
-            aslot += 2;
-            if (aslot >= kASlots) {
-                aslot -= kASlots;
-                apar ^= 1u;
-            }
+            ++a_q;
         }
     } else if (warp >= kFirstIssuer) {
         // --------------------------------------------------------- MMA issuers
@@ -336,14 +321,12 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
         // field is advanced by adding operand offsets (addresses stay below
         // 256 KB, so the 14-bit field never carries).
         const int k_iss = warp - kFirstIssuer;
-        const int cp = k_iss >> 1;
         if (lane == 0 && any) {
             int gc = 0, aslot = 0;
             uint32_t apar = 0;
             bool ok = true;
             const uint32_t a_col = tmem + (uint32_t)(k_iss * 32);
-            const uint32_t af0 = bars + kBarAFull + 8u * (uint32_t)cp;   // slot a: + 8 * kPairs * a
-            const uint32_t ae0 = bars + kBarAEmpty + 8u * (uint32_t)cp;
+            const uint32_t af0 = bars + kBarAFull, ae0 = bars + kBarAEmpty;  // slot a: + 8a
             while (ok) {
                 const int buf = gc & 1;
                 const uint32_t d = tmem + kDCol + 16u * (uint32_t)(kIssuers * buf + k_iss);
@@ -360,7 +343,7 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                 const int n_st = cur.n_stages_chunk;
                 uint64_t bd = bd0;
                 for (int st = 0; st < n_st; ++st, bd += st_step) {
-                    const uint32_t af = af0 + (uint32_t)(8 * kPairs * aslot);
+                    const uint32_t af = af0 + (uint32_t)(8 * aslot);
                     if (!ptx::mbar_try_wait(af, apar) && !waiter.wait(af, apar)) {
                         ok = false;
                         break;
@@ -371,7 +354,7 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
 #pragma unroll
                     for (int t = 1; t < 4; ++t)  // K=32 step 4k+t: A columns +8t, B words +2t
                         ptx::mma_ts_f8f6f4(d, a + 8u * t, bd + (uint64_t)(t_step * t), kIdesc, 1u);
-                    ptx::mma_commit(ae0 + (uint32_t)(8 * kPairs * aslot));
+                    ptx::mma_commit(ae0 + (uint32_t)(8 * aslot));
                     const bool wrap = aslot == kASlots - 1;
                     aslot = wrap ? 0 : aslot + 1;
                     apar ^= wrap ? 1u : 0u;
@@ -663,7 +646,6 @@ tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t strea
         begin = end;
         if (cnt == 0) continue;
         prm.n_items = cnt;
-        prm.zero = 0u;
         // contiguous runs of units with balanced stage counts
         const int ctas = units < sms ? units : (sms < kMaxCtas ? sms : kMaxCtas);
         long long total = 0;
