@@ -341,7 +341,8 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                 const uint64_t bd0 = b_desc_lbo(bbuf + (uint32_t)buf * kBBufStride + (uint32_t)(8 * k_iss) * wbytes, wbytes);
                 const uint32_t st_step = (kStageWords * wbytes) >> 4, t_step = (2u * wbytes) >> 4;
                 const int n_st = cur.n_stages_chunk;
-                uint64_t bd = bd0;
+                const uint32_t bd_hi = (uint32_t)(bd0 >> 32);  // only the start address (low half) advances
+                uint32_t bd = (uint32_t)bd0;
                 for (int st = 0; st < n_st; ++st, bd += st_step) {
                     const uint32_t af = af0 + (uint32_t)(8 * aslot);
                     if (!ptx::mbar_try_wait(af, apar) && !waiter.wait(af, apar)) {
@@ -350,10 +351,10 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                     }
                     ptx::tc_fence_after();
                     const uint32_t a = a_col + (uint32_t)(aslot * 128);
-                    ptx::mma_ts_f8f6f4(d, a, bd, kIdesc, st != 0 ? 1u : 0u);
+                    ptx::mma_ts_f8f6f4_lh(d, a, bd, bd_hi, kIdesc, st != 0 ? 1u : 0u);
 #pragma unroll
                     for (int t = 1; t < 4; ++t)  // K=32 step 4k+t: A columns +8t, B words +2t
-                        ptx::mma_ts_f8f6f4(d, a + 8u * t, bd + (uint64_t)(t_step * t), kIdesc, 1u);
+                        ptx::mma_ts_f8f6f4_lh(d, a + 8u * t, bd + t_step * t, bd_hi, kIdesc, 1u);
                     ptx::mma_commit(ae0 + (uint32_t)(8 * aslot));
                     const bool wrap = aslot == kASlots - 1;
                     aslot = wrap ? 0 : aslot + 1;

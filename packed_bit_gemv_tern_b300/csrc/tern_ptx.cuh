@@ -166,6 +166,20 @@ __device__ __forceinline__ void mma_ts_f8f6f4(uint32_t d_tmem, uint32_t a_tmem, 
         : "memory");
 }
 
+// As mma_ts_f8f6f4, with the B descriptor given as its two 32-bit halves
+// (callers that walk a buffer advance only the low half).
+__device__ __forceinline__ void mma_ts_f8f6f4_lh(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t b_hi,
+                                                 uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 bd;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "mov.b64 bd, {%2, %3};\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], bd, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b_lo), "r"(b_hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Arrive once on an mbarrier when every prior tcgen05 async op of this thread completes.
 __device__ __forceinline__ void mma_commit(uint32_t bar)
 {
