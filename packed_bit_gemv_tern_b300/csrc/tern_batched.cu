@@ -49,12 +49,11 @@ using namespace mma;
 constexpr int kMaxItems = 128;             // items per launch (kernel parameter space)
 constexpr int kMaxMaps = 144;              // tensor maps per launch: one per item, two per SwiGLU pair
 constexpr int kMaxCtas = 160;
-constexpr int kThreads = 672;              // 21 warps
+constexpr int kThreads = 544;              // 17 warps
 constexpr int kFirstStager = 1;            // warps 1-4
 constexpr int kStagers = 128;
 constexpr int kFirstDec = 5;               // warps 5-16: three decoder groups of four warps
-constexpr int kFirstIssuer = 17;           // warps 17-20: issuer k = chunk column k
-constexpr int kIssuers = 4;
+constexpr int kCols = 4;                   // chunk columns of a stage; warp q of a group issues column q
 // Decoder group g decodes the stages s = g (mod 3) into TMEM slot g and ring
 // slots g and g + 3: every slot a group waits on was last used by the group
 // itself, so a phase-parity wait can never be two phases ahead (which would
@@ -62,7 +61,7 @@ constexpr int kIssuers = 4;
 constexpr int kDecGroups = 3;
 constexpr int kASlots = 3;                 // TMEM A slots, one stage (128 columns) each
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kDCol = kASlots * 128;  // D[buf][k] at kDCol + 16 * (kIssuers * buf + k)
+constexpr uint32_t kDCol = kASlots * 128;  // D[buf][k] at kDCol + 16 * (kCols * buf + k)
 // B buffer of one chunk in the compact layout: the 2m rows (hi/lo of each
 // activation row) of a 16-code block are contiguous, blocks 32m bytes apart.
 // The MMA reads eight rows of a core matrix from each block start and eight
@@ -112,14 +111,14 @@ constexpr uint32_t kOffXch = kOffB + 2 * kBBufStride;  // [64][8] fp32
 constexpr uint32_t kOffBar = kOffXch + 64 * 8 * 4;
 constexpr uint32_t kBarWFull = 0;                       // [kWStages]
 constexpr uint32_t kBarWEmpty = kBarWFull + 8 * kWStages;
-constexpr uint32_t kBarAFull = kBarWEmpty + 8 * kWStages;  // [kASlots]
-constexpr uint32_t kBarAEmpty = kBarAFull + 8 * kASlots;
-constexpr uint32_t kBarBFull = kBarAEmpty + 8 * kASlots;    // [2]
+constexpr uint32_t kBarAEmpty = kBarWEmpty + 8 * kWStages;  // [kASlots]: the slot's MMAs are done
+constexpr uint32_t kBarBFull = kBarAEmpty + 8 * kASlots;     // [2]
 constexpr uint32_t kBarBEmpty = kBarBFull + 16;
 constexpr uint32_t kBarDFull = kBarBEmpty + 16;
 constexpr uint32_t kBarDEmpty = kBarDFull + 16;
-constexpr uint32_t kBarDrain = kBarDEmpty + 16;  // one commit per issuer on exit
-constexpr uint32_t kWordsOff = kBarDrain + 8;
+constexpr uint32_t kBarDrain = kBarDEmpty + 16;  // one commit per issuing warp on exit
+constexpr uint32_t kBarTurn = kBarDrain + 8;     // [kCols][kDecGroups]: group g's turn on column q
+constexpr uint32_t kWordsOff = kBarTurn + 8 * kCols * kDecGroups;
 // words: [0] tmem base, [1] abort, [8..15] xmax buffer 0, [16..23] xmax buffer 1
 constexpr uint32_t kSmemBytes = 1024 + kOffBar + kWordsOff + 32 * 4;
 
@@ -196,17 +195,15 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
             ptx::mbar_init(bars + kBarWFull + 8 * s, 1);
             ptx::mbar_init(bars + kBarWEmpty + 8 * s, 4 * 32);  // every lane of the stage's decoder group
         }
-        for (int s = 0; s < kASlots; ++s) {
-            ptx::mbar_init(bars + kBarAFull + 8 * s, 4 * 32);  // every lane of the decoding group
-            ptx::mbar_init(bars + kBarAEmpty + 8 * s, kIssuers);
-        }
+        for (int s = 0; s < kASlots; ++s) ptx::mbar_init(bars + kBarAEmpty + 8 * s, kCols);  // the group's issuing lanes
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(bars + kBarBFull + 8 * b, kStagers);  // every staging thread, after its proxy fence
-            ptx::mbar_init(bars + kBarBEmpty + 8 * b, kIssuers);
-            ptx::mbar_init(bars + kBarDFull + 8 * b, kIssuers);
+            ptx::mbar_init(bars + kBarBEmpty + 8 * b, kCols);  // the issuing lanes of the chunk's last stage
+            ptx::mbar_init(bars + kBarDFull + 8 * b, kCols);
             ptx::mbar_init(bars + kBarDEmpty + 8 * b, 4);
         }
-        ptx::mbar_init(bars + kBarDrain, kIssuers);
+        ptx::mbar_init(bars + kBarDrain, kDecGroups * kCols);
+        for (int j = 0; j < kCols * kDecGroups; ++j) ptx::mbar_init(bars + kBarTurn + 8 * j, 1);
         for (int j = 1; j < 32; ++j) words[j] = 0u;
         ptx::fence_proxy_async_smem();
     }
@@ -257,115 +254,112 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
             for (int s = gs > kWStages ? gs - kWStages : 0; s < gs; ++s)
                 drain_wait(bars + kBarWFull + 8 * (s % kWStages), (s / kWStages) & 1, &g_batched_error);
         }
-    } else if (warp >= kFirstDec && warp < kFirstIssuer) {
-        // --------------------------------------------------------- decoders
+    } else if (warp >= kFirstDec) {
+        // ----------------------------------------- decoders and MMA issuers
         // Group g decodes all four columns of the stages s = g (mod 3) into
-        // TMEM slot g; quad q owns TMEM lanes 32q..32q+31.  Three decoder
-        // warps share each scheduler, so one warp's barrier round trips hide
-        // behind the others' decoding, and a warp's control work is paid once
-        // per stage it decodes.  Every lane arrives on the
-        // barriers (no divergent single-lane path).  The ring slot is released
-        // after the last TMEM store, which consumes the last loaded words.
+        // TMEM slot g (quad q owns TMEM lanes 32q..32q+31), the group meets
+        // at a named barrier, and then warp q issues the four K=32 steps of
+        // column q (tcgen05.mma kind::f8f6f4, A from TMEM, B from shared
+        // memory, M = 128, N = 16) into D[buf][q].  Stage s's MMAs on a column
+        // follow stage s-1's, issued by the previous group, through that
+        // column's turn barriers (tcgen05 fence, mbarrier, fence), which order
+        // the accumulation; a warp issues for one stage in three, so one
+        // thread's waits and bookkeeping overlap the others' MMA issue (a
+        // warp issues an MMA about every 54 cycles, warps overlap).  Every
+        // slot a group waits on was last used by the group itself, so no
+        // phase-parity wait runs two phases ahead of its barrier.  A chunk's
+        // first-stage issuers wait for its B and D buffers (later stages see
+        // them through the turn chain); its last-stage issuers commit the
+        // chunk's D and B, which tracks the whole accumulation chain.
         const int g = (warp - kFirstDec) >> 2;
         const int quad = warp & 3;
         const int i = quad * 32 + lane;
         const uint32_t tm_row = tmem + ((uint32_t)(quad * 32) << 16);
         const uint32_t row_addr = wbuf + (uint32_t)i * 128u;
         const uint32_t sw = (uint32_t)(i & 7);  // 128-byte swizzle: 16-byte chunk c of row i sits at c ^ (i & 7)
-        const int total = any ? p.stages_cta[blockIdx.x] : 0;
+        const uint32_t a_col = tmem + (uint32_t)(g * 128 + quad * 32);  // column q of slot g (lane 0)
+        const uint32_t my_turn = bars + kBarTurn + 8u * (uint32_t)(kDecGroups * quad + g);
+        const uint32_t next_turn = bars + kBarTurn + 8u * (uint32_t)(kDecGroups * quad + (g + 1) % kDecGroups);
+        const uint32_t a_empty = bars + kBarAEmpty + 8u * (uint32_t)g;
+        const uint32_t bar_id = 2u + (uint32_t)g;  // 0: __syncthreads, 1: staging warps
         static_assert(kWStages % kDecGroups == 0 && kASlots == kDecGroups, "slots must cycle within a group");
-        int w_r = g, w_q = 0;  // stage s: ring slot s % kWStages, use s / kWStages
-        int a_q = 0;           //          TMEM slot g = s % kASlots, use s / kASlots
-        const int a_r = g;
-        for (int s = g; s < total; s += kDecGroups) {
-            const uint32_t wf = bars + kBarWFull + 8 * w_r;
-            const uint32_t ae = bars + kBarAEmpty + 8 * a_r;
-            const uint32_t wpar = (uint32_t)w_q & 1u, apar = (uint32_t)a_q & 1u;
-            // both fast-path tests issue back to back; the bounded waits only on a miss
-            bool okw = ptx::mbar_try_wait(wf, wpar);
-            bool oka = ptx::mbar_try_wait(ae, apar ^ 1u);
-            if (!okw) okw = waiter.wait(wf, wpar);
-            if (okw && !oka) oka = waiter.wait(ae, apar ^ 1u);
-            if (!__all_sync(0xFFFFFFFFu, okw && oka)) break;
-            ptx::tc_fence_after();
-            const uint32_t srow = row_addr + (uint32_t)w_r * kStageBytes;
-            const uint32_t ta = tm_row + (uint32_t)(a_r * 128);
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-                const uint4 v0 = ptx::lds128(srow + ((((uint32_t)(2 * c)) ^ sw) << 4));
-                const uint4 v1 = ptx::lds128(srow + ((((uint32_t)(2 * c + 1)) ^ sw) << 4));
-                uint32_t r[32];
-                decode8(v0, v1, r);
-                ptx::tmem_st_32x32b_x32(ta + 32u * (uint32_t)c, r);
-            }
-            ptx::mbar_arrive(bars + kBarWEmpty + 8 * w_r);
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bars + kBarAFull + 8 * a_r);
-            w_r += kDecGroups;  // s += 3
-            if (w_r >= kWStages) {
-                w_r -= kWStages;
-                ++w_q;
-            }
-            ++a_q;
-        }
-    } else if (warp >= kFirstIssuer) {
-        // --------------------------------------------------------- MMA issuers
-        // Issuer k runs the K=32 steps of chunk column k (steps 4k..4k+3 of
-        // every stage) into its own accumulator of the chunk's D buffer.  The
-        // issuing thread shares its scheduler with four busy decoder warps,
-        // so its per-stage path is kept to the barrier test, the fence, the
-        // four MMAs and the commit: the chunk's stage loop is unrolled, and
-        // slots, parities, barrier addresses and descriptor offsets are
-        // formed from the chunk start.  The B descriptor's start-address
-        // field is advanced by adding operand offsets (addresses stay below
-        // 256 KB, so the 14-bit field never carries).
-        const int k_iss = warp - kFirstIssuer;
-        if (lane == 0 && any) {
-            int gc = 0, aslot = 0;
-            uint32_t apar = 0;
-            bool ok = true;
-            const uint32_t a_col = tmem + (uint32_t)(k_iss * 32);
-            const uint32_t af0 = bars + kBarAFull, ae0 = bars + kBarAEmpty;  // slot a: + 8a
-            while (ok) {
-                const int buf = gc & 1;
-                const uint32_t d = tmem + kDCol + 16u * (uint32_t)(kIssuers * buf + k_iss);
-                const uint32_t bfull = bars + kBarBFull + 8 * buf, dempty = bars + kBarDEmpty + 8 * buf;
-                const uint32_t bpar = (uint32_t)(gc >> 1) & 1u;
-                ok = (ptx::mbar_try_wait(bfull, bpar) || waiter.wait(bfull, bpar)) &&
-                     (ptx::mbar_try_wait(dempty, bpar ^ 1u) || waiter.wait(dempty, bpar ^ 1u));
-                if (!ok) break;
-                ptx::tc_fence_after();
-                // compact B: 16-code blocks 32m bytes apart; column k starts at word 8k
-                const uint32_t wbytes = 32u * (uint32_t)p.item[cur.item].m;
-                const uint64_t bd0 = b_desc_lbo(bbuf + (uint32_t)buf * kBBufStride + (uint32_t)(8 * k_iss) * wbytes, wbytes);
-                const uint32_t st_step = (kStageWords * wbytes) >> 4, t_step = (2u * wbytes) >> 4;
-                const int n_st = cur.n_stages_chunk;
-                const uint32_t bd_hi = (uint32_t)(bd0 >> 32);  // only the start address (low half) advances
-                uint32_t bd = (uint32_t)bd0;
-                for (int st = 0; st < n_st; ++st, bd += st_step) {
-                    const uint32_t af = af0 + (uint32_t)(8 * aslot);
-                    if (!ptx::mbar_try_wait(af, apar) && !waiter.wait(af, apar)) {
-                        ok = false;
-                        break;
-                    }
+        int w_r = g, w_q = 0;      // stage s: ring slot s % kWStages, use s / kWStages
+        int a_q = 0;               //          TMEM slot g, use s / kASlots
+        uint32_t tpar = g == 0 ? 1u : 0u;  // stage 0 needs no turn
+        int gs = 0, gc = 0;
+        bool more = any;
+        while (more) {
+            const int n_st = cur.n_stages_chunk;
+            const int buf = gc & 1;
+            const uint32_t wbytes = 32u * (uint32_t)p.item[cur.item].m;
+            for (int st = (g - gs % kDecGroups + kDecGroups) % kDecGroups; st < n_st; st += kDecGroups) {
+                const uint32_t wf = bars + kBarWFull + 8 * w_r;
+                const uint32_t wpar = (uint32_t)w_q & 1u, apar = (uint32_t)a_q & 1u;
+                // both fast-path tests issue back to back; the bounded waits only on a miss
+                bool okw = ptx::mbar_try_wait(wf, wpar);
+                bool oka = ptx::mbar_try_wait(a_empty, apar ^ 1u);
+                if (!okw) okw = waiter.wait(wf, wpar);
+                if (okw && !oka) oka = waiter.wait(a_empty, apar ^ 1u);
+                if (__all_sync(0xFFFFFFFFu, okw && oka)) {
                     ptx::tc_fence_after();
-                    const uint32_t a = a_col + (uint32_t)(aslot * 128);
-                    ptx::mma_ts_f8f6f4_lh(d, a, bd, bd_hi, kIdesc, st != 0 ? 1u : 0u);
-#pragma unroll
-                    for (int t = 1; t < 4; ++t)  // K=32 step 4k+t: A columns +8t, B words +2t
-                        ptx::mma_ts_f8f6f4_lh(d, a + 8u * t, bd + t_step * t, bd_hi, kIdesc, 1u);
-                    ptx::mma_commit(ae0 + (uint32_t)(8 * aslot));
-                    const bool wrap = aslot == kASlots - 1;
-                    aslot = wrap ? 0 : aslot + 1;
-                    apar ^= wrap ? 1u : 0u;
+                    const uint32_t srow = row_addr + (uint32_t)w_r * kStageBytes;
+                    const uint32_t ta = tm_row + (uint32_t)(g * 128);
+#pragma unroll 1
+                    for (int c = 0; c < 4; ++c) {
+                        const uint4 v0 = ptx::lds128(srow + ((((uint32_t)(2 * c)) ^ sw) << 4));
+                        const uint4 v1 = ptx::lds128(srow + ((((uint32_t)(2 * c + 1)) ^ sw) << 4));
+                        uint32_t r[32];
+                        decode8(v0, v1, r);
+                        ptx::tmem_st_32x32b_x32(ta + 32u * (uint32_t)c, r);
+                    }
+                    ptx::mbar_arrive(bars + kBarWEmpty + 8 * w_r);  // after the last store, which consumed the loads
+                    ptx::tmem_wait_st();
                 }
-                if (!ok) break;
-                ptx::mma_commit(bars + kBarDFull + 8 * buf);
-                ptx::mma_commit(bars + kBarBEmpty + 8 * buf);
-                ++gc;
-                ok = cur.next_chunk();
+                ptx::tc_fence_before();
+                // the group's 128 rows are in TMEM; stop together on an abort
+                if (ptx::named_bar_or(bar_id, 128, *abort_flag != 0u)) {
+                    more = false;
+                    break;
+                }
+                if (lane == 0) {
+                    const uint32_t bpar = (uint32_t)(gc >> 1) & 1u;
+                    const uint32_t bfull = bars + kBarBFull + 8 * buf, dempty = bars + kBarDEmpty + 8 * buf;
+                    bool lok = st != 0 || ((ptx::mbar_try_wait(bfull, bpar) || waiter.wait(bfull, bpar)) &&
+                                           (ptx::mbar_try_wait(dempty, bpar ^ 1u) || waiter.wait(dempty, bpar ^ 1u)));
+                    lok = lok && (ptx::mbar_try_wait(my_turn, tpar) || waiter.wait(my_turn, tpar));
+                    if (lok) {
+                        ptx::tc_fence_after();
+                        const uint32_t d = tmem + kDCol + 16u * (uint32_t)(kCols * buf + quad);
+                        // compact B: 16-code blocks 32m bytes apart; column q of stage st at word st*32 + 8q
+                        const uint64_t bd = b_desc_lbo(bbuf + (uint32_t)buf * kBBufStride +
+                                                           (uint32_t)(st * kStageWords + 8 * quad) * wbytes,
+                                                       wbytes);
+                        const uint32_t bd_lo = (uint32_t)bd, bd_hi = (uint32_t)(bd >> 32), t_step = (2u * wbytes) >> 4;
+                        ptx::mma_ts_f8f6f4_lh(d, a_col, bd_lo, bd_hi, kIdesc, st != 0 ? 1u : 0u);
+#pragma unroll
+                        for (int t = 1; t < 4; ++t)  // K=32 step 4q+t: A columns +8t, B words +2t
+                            ptx::mma_ts_f8f6f4_lh(d, a_col + 8u * t, bd_lo + t_step * t, bd_hi, kIdesc, 1u);
+                        ptx::tc_fence_before();
+                        ptx::mbar_arrive(next_turn);  // the next stage's MMAs on this column follow these
+                        ptx::mma_commit(a_empty);
+                        if (st == n_st - 1) {
+                            ptx::mma_commit(bars + kBarDFull + 8 * buf);
+                            ptx::mma_commit(bars + kBarBEmpty + 8 * buf);
+                        }
+                    }
+                }
+                __syncwarp();
+                tpar ^= 1u;
+                w_r += kDecGroups;  // s += 3
+                if (w_r >= kWStages) {
+                    w_r -= kWStages;
+                    ++w_q;
+                }
+                ++a_q;
             }
+            gs += n_st;
+            ++gc;
+            more = more && cur.next_chunk();
         }
         // arrives once every MMA this thread issued has completed (at once if none)
         if (lane == 0) ptx::mma_commit(bars + kBarDrain);
@@ -398,9 +392,9 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
             if (good) {
                 ptx::tc_fence_after();
 #pragma unroll 1
-                for (int a = 0; a < kIssuers; ++a) {
+                for (int a = 0; a < kCols; ++a) {
                     uint32_t dv[16];
-                    ptx::tmem_ld_32x32b_x16(tmem + ((uint32_t)(quad * 32) << 16) + kDCol + 16u * (kIssuers * eb + a), dv);
+                    ptx::tmem_ld_32x32b_x16(tmem + ((uint32_t)(quad * 32) << 16) + kDCol + 16u * (kCols * eb + a), dv);
                     ptx::tmem_wait_ld();
 #pragma unroll
                     for (int n = 0; n < 16; ++n) dsum[n] += __uint_as_float(dv[n]);
@@ -455,11 +449,10 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
             uint32_t *xm = words + 8 + 8 * buf;
             const bool reuse = held_item[buf] == cur.item && held_chunk[buf] == cur.chunk;
             // Past this barrier every staging warp has finished chunk gc-2's
-            // epilogue, the last reader of this buffer's row maxima xm.  A
-            // failed wait has raised the abort flag before it, so all four
-            // staging warps take the same branch after it.
-            ptx::named_bar_sync(1, kStagers);
-            if (*abort_flag) break;
+            // epilogue, the last reader of this buffer's row maxima xm.  The
+            // barrier ORs the abort flag over the four staging warps, so they
+            // all take the same branch.
+            if (ptx::named_bar_or(1, kStagers, *abort_flag != 0u)) break;
             if (reuse) {  // B (and its row scales) already hold this chunk
                 ptx::mbar_arrive(bars + kBarBFull + 8 * buf);
                 if (gc >= 1) epilogue(gc - 1);
@@ -521,7 +514,7 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
             ++gc;
             ok = cur.next_chunk();
         }
-        if (gc >= 1 && !*abort_flag) epilogue(gc - 1);
+        if (!ptx::named_bar_or(1, kStagers, *abort_flag != 0u) && gc >= 1) epilogue(gc - 1);
     }
 
     __syncthreads();

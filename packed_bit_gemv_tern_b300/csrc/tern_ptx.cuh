@@ -259,5 +259,22 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t threads)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Named barrier that also ORs a predicate over the participating threads:
+// every thread gets the same answer, so a decision taken on it (to stop on
+// an abort flag, say) is uniform across the warps that meet there.
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t threads, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %3, 0;\n\t"
+        "bar.red.or.pred p, %1, %2, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"(id), "r"(threads), "r"(v ? 1u : 0u)
+        : "memory");
+    return r != 0u;
+}
+
 }  // namespace ptx
 }  // namespace tern
