@@ -448,6 +448,10 @@ tern_status launch_mma(const tern_matrix *g, const tern_matrix *u, const uint16_
         n_wst = fixed < (uint32_t)kSmemLimit ? (int)((kSmemLimit - fixed) / kStageBytes) : 0;
         if (n_wst > kMaxWStages) n_wst = kMaxWStages;
         if (n_wst > per_st && per_st >= 1) n_wst = per_st < 2 ? 2 : per_st;  // no deeper than the work
+        // Even depth: the two decoder warpgroups take alternate stages, so a
+        // ring slot is then always reused by the group that last used it and
+        // a phase-parity wait never runs two phases ahead of its barrier.
+        n_wst &= ~1;
         if (n_wst >= 2 || split >= 8) break;
         split *= 2;
     }
