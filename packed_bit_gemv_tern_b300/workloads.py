@@ -220,5 +220,22 @@ def _pack_io(wl: Workload, device):
     wl.x_flat, wl.y_flat = xf, yf
 
 
+def io_copy(wl: Workload):
+    """A second set of activation and output buffers for the calls of `wl`
+    (same weights, same shapes and layout as wl.x_flat / wl.y_flat) and the
+    batch that uses them, so a caller can prepare one step's inputs while
+    another step runs.  Returns (x_flat, y_flat, batch, items)."""
+    import torch
+    xf = torch.empty_like(wl.x_flat)
+    yf = torch.zeros_like(wl.y_flat)
+    items, ox, oy = [], 0, 0
+    for c in wl.calls:
+        nx, ny = c.x.numel(), c.y.numel()
+        items.append((c.w, c.up, xf[ox:ox + nx].view(c.x.shape), yf[oy:oy + ny].view(c.y.shape), c.m))
+        ox += nx
+        oy += ny
+    return xf, yf, batch_items(items), items
+
+
 def _clone(w: TernMatrix) -> TernMatrix:
     return TernMatrix(w.codes.clone(), w.scale.clone(), w.k, None if w.rowsum is None else w.rowsum.clone())
