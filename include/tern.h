@@ -165,13 +165,25 @@ typedef struct {
  * over the fewest that fit; an item with k == 0 (y = 0) takes a small launch
  * of its own and one with rows == 0 none.  Tensor maps of the weights are
  * encoded once per (codes, shape) and cached by the library, so repeated
- * calls on resident weights cost a lookup on the host.  n == 0 is a no-op; items == NULL gives TERN_ERR_NULL,
+ * calls on resident weights cost a lookup on the host.
+ * Workspace: when a launch group holds items with m >= 2, a short kernel
+ * runs just before it and writes those items' activations, split into the
+ * operand form the tensor cores read, to a device workspace that the library
+ * owns: one per (device, stream), allocated with cudaMalloc on first need
+ * (also while the stream is being captured), grown by doubling and never
+ * freed, since a captured launch keeps its address.  Launches on one stream
+ * are ordered, so they share it safely; a captured graph must not run at the
+ * same time as other calls on the stream it was captured on.  If the
+ * allocation fails, the persistent kernel builds the operand itself (slower,
+ * same results).  n == 0 is a no-op; items == NULL gives TERN_ERR_NULL,
  * n < 0 TERN_ERR_SHAPE. */
 TERN_API tern_status tern_gemm_batched(const tern_batch_item *items, int32_t n, void *stream);
 
 /* Number of kernel launches tern_gemm_batched makes for these items (host
  * only, nothing is launched and only items[i].w->rows and ->k are read; the
- * items are not otherwise checked).  0 for n == 0; a negative tern_status for
+ * items are not otherwise checked), counting the activation-preparing
+ * launch of each group that holds items with m >= 2.  0 for n == 0; a
+ * negative tern_status for
  * n < 0 (-TERN_ERR_SHAPE) or a NULL items array or weight pointer
  * (-TERN_ERR_NULL).  Not an operation of the model pages: a planning aid for
  * callers that count or capture launches. */

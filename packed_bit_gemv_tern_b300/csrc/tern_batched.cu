@@ -7,25 +7,30 @@
 // a unit is one 128-row tile (64 gate + 64 up rows for a SwiGLU pair) of one
 // item over the item's whole K, so no unit needs a cross-CTA reduction.  The
 // host balances the runs by packed bytes.  K is processed in chunks of up to
-// 16384 / m codes (the whole K for m = 1 at every Neutrino shape); the B
-// operand (activations as two e4m3 terms under a per-row power-of-two scale,
-// see split_pair) and the fp32 accumulators are double buffered per chunk, a
-// chunk's B is reused by every later tile of the item on the same buffer, and
-// staging the next chunk's activations and reading the
-// previous chunk's sums overlap the weight stream.  Roles (21 warps):
+// 28672 / m codes (the whole K for m = 1 at every Neutrino shape); the B
+// operand (activations as two e4m3 terms under a per-row power-of-two scale
+// per chunk, see split_pair) and the fp32 accumulators are double buffered
+// per chunk, a chunk's B is reused by every later tile of the item on the
+// same buffer, and fetching the next chunk's B and reading the previous
+// chunk's sums overlap the weight stream.  Roles (17 warps):
 //   * warp 0, lane 0: TMA producer; streams every stage of every unit of the
 //     CTA through a 6-deep ring of 16 KB stages (128 rows x 512 codes,
 //     128-byte swizzle), never waiting on activations.
-//   * warps 1-4: stage B for each chunk (after griddepcontrol.wait), then read
-//     the previous chunk's accumulators, rescale and add them into per-row
-//     registers, and at the end of a unit write y (scale, SiLU gate).
+//   * warps 1-4: bring in B for each chunk (after griddepcontrol.wait), then
+//     read the previous chunk's accumulators, rescale and add them into
+//     per-row registers, and at the end of a unit write y (scale, SiLU gate).
+//     For m = 1 they build B from x themselves; for m >= 2 a short kernel
+//     launched just before (k_tern_bprep) has written every chunk's B and row
+//     maxima to a workspace once, and a chunk is one bulk copy: building it
+//     in every CTA that streams a tile of the item costs more than the
+//     chunk's weight stream when m is large.
 //   * warps 5-16: three decoder groups of four warps; group g turns the four
 //     chunk columns (128 codes of a row each) of the stages s = g (mod 3)
-//     into e4m3 +-2/0 bytes (decode8) in TMEM slot g.  Three decoder warps
+//     into e4m3 +-2/0 bytes (decode8) in TMEM slot g, and lane 0 of warp q
+//     of the group then issues the K=32 steps of column q (tcgen05.mma
+//     kind::f8f6f4, A from TMEM, B from shared memory, M = 128, N = 16) into
+//     the column's accumulator of the chunk's buffer.  Three decoder warps
 //     per scheduler hide each other's barrier latency.
-//   * warps 17-20, lane 0: MMA issuers; issuer k runs the K=32 steps of column
-//     k (tcgen05.mma kind::f8f6f4, A from TMEM, B from shared memory,
-//     M = 128, N = 16) into its own accumulator of the chunk's buffer.
 // Every mbarrier wait is bounded; on time-out the kernel records the error,
 // stops, drains its copies and MMAs, releases its tensor memory and returns.
 #include <cuda.h>
@@ -33,6 +38,9 @@
 
 #include <cstdint>
 #include <cstring>
+#include <map>
+#include <mutex>
+#include <utility>
 #include <vector>
 
 #include "tern.h"
@@ -88,14 +96,21 @@ struct Item {
     float *y;
     int rows, k, m, swiglu;
     int stages;  // 512-code stages over K
-    int cstages; // stages per K chunk: min(stages, 32 / m), so a chunk's B fits one buffer
+    int cstages; // stages per K chunk (the last may be shorter); a chunk's B fits one buffer
     int unit0;   // first global unit of this item
     int map;     // its codes' tensor map (gate, then up, for a SwiGLU pair)
+    // B prepared by k_tern_bprep (nullptr: the staging warps build it): word
+    // w of row i of the item's padded K at byte w * 32m + 32i (hi row, then
+    // lo row), so chunk c is the contiguous range from c * cstages * 1024m;
+    // xmax[8c + i] = the row maximum (fp32 bits of |x|) over chunk c.
+    const unsigned char *bsrc;
+    const uint32_t *xmax;
 };
 
 struct Params {
     int n_items;
     int unit_start[kMaxCtas + 1];  // CTA b runs units [unit_start[b], unit_start[b + 1])
+    int item_start[kMaxCtas];      // the item holding unit unit_start[b]
     int stages_cta[kMaxCtas];      // 512-code stages in CTA b's run
     Item item[kMaxItems];
 };
@@ -145,8 +160,7 @@ struct Cursor {
         unit = p->unit_start[b];
         unit_end = p->unit_start[b + 1];
         if (unit >= unit_end) return false;
-        item = 0;
-        while (item + 1 < p->n_items && p->item[item + 1].unit0 <= unit) ++item;
+        item = p->item_start[b];
         enter_item();
         tile = unit - p->item[item].unit0;
         chunk = 0;
@@ -173,6 +187,85 @@ struct Cursor {
     }
     __device__ bool last_chunk_of_unit() const { return chunk + 1 == n_chunks; }
 };
+
+// ------------------------------------------------------------------ B prep
+// One CTA per (item, chunk, activation row) of the items with m >= 2: the
+// row's largest |x| over the chunk, then every word (16 k) of the chunk split
+// into its hi and lo e4m3 rows at the row's scale (split_word), written in
+// the compact layout the MMA reads (Item::bsrc).  Words past K are zeros.
+// The result is the same, byte for byte, as the staging warps' own build.
+// A chunk holds at most 28 stages (m = 2), so each thread keeps its words in
+// registers between the two passes and all loads are in flight at once.
+constexpr int kPrepThreads = 128;
+constexpr int kPrepWords = 7;           // words per thread: 28 stages * 32 / 128
+constexpr uint32_t kBulkPiece = 16384;  // bytes per bulk copy of a prepared chunk
+
+struct PrepItem {
+    const uint16_t *x;
+    unsigned char *b;
+    uint32_t *xmax;
+    int k, m, stages, cstages;
+    int task0;  // first task of the item; task task0 + c * m + i is chunk c, row i
+};
+
+struct PrepParams {
+    int n_items, n_tasks;
+    PrepItem item[kMaxItems];
+};
+
+__global__ void __launch_bounds__(kPrepThreads) k_tern_bprep(const __grid_constant__ PrepParams p)
+{
+    __shared__ uint32_t wmax[kPrepThreads / 32];
+    // The persistent kernel that follows may start at once: its weight stream
+    // needs nothing from here, and its staging warps wait for this grid to
+    // finish before they read the workspace.  (A prep CTA fits on an SM
+    // beside a persistent CTA.)  The previous kernel on the stream may still
+    // read the workspace, and x may come from it: wait for it.
+    ptx::grid_dep_launch();
+    ptx::grid_dep_wait();
+    const int tid = (int)threadIdx.x, task = (int)blockIdx.x;
+    int j = 0;
+    while (j + 1 < p.n_items && p.item[j + 1].task0 <= task) ++j;
+    const PrepItem &it = p.item[j];
+    const int local = task - it.task0, c = local / it.m, mm = local - c * it.m;
+    const int w0 = c * it.cstages * kStageWords;
+    const int nw = min(it.cstages, it.stages - c * it.cstages) * kStageWords;
+    const int kw = it.k / 16;
+    const uint4 *xr = reinterpret_cast<const uint4 *>(it.x + (size_t)mm * it.k);  // 2 x uint4 per word
+    uint4 va[kPrepWords], vb[kPrepWords];
+    uint32_t mx = 0;
+#pragma unroll
+    for (int q = 0; q < kPrepWords; ++q) {
+        const int wi = tid + q * kPrepThreads, gw = w0 + wi;
+        va[q] = vb[q] = make_uint4(0u, 0u, 0u, 0u);
+        if (wi < nw && gw < kw) {
+            va[q] = __ldg(xr + 2 * gw);
+            vb[q] = __ldg(xr + 2 * gw + 1);
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < kPrepWords; ++q) mx = max(mx, max_abs16(va[q], vb[q]));
+    mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+    if ((tid & 31) == 0) wmax[tid >> 5] = mx;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kPrepThreads / 32; ++w) mx = max(mx, wmax[w]);
+    if (tid == 0) it.xmax[8 * c + mm] = mx;
+    const float sc = exp2i(row_scale_exp(mx));
+    const size_t wbytes = 32u * (size_t)it.m;
+    unsigned char *dst = it.b + (size_t)w0 * wbytes + 32u * (size_t)mm;
+#pragma unroll
+    for (int q = 0; q < kPrepWords; ++q) {
+        const int wi = tid + q * kPrepThreads;
+        if (wi < nw) {
+            uint4 hi4, lo4;
+            split_word(va[q], vb[q], sc, hi4, lo4);
+            uint4 *d = reinterpret_cast<uint4 *>(dst + (size_t)wi * wbytes);
+            d[0] = hi4;
+            d[1] = lo4;
+        }
+    }
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps maps)
@@ -380,6 +473,7 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
         // what each B buffer holds: a chunk of an item is staged once and reused
         // by every later tile of the same item that lands on this buffer
         int held_item[2] = {-1, -1}, held_chunk[2] = {-1, -1};
+        int last_gc[2] = {-1, -1};  // last chunk whose BFull phase each buffer took part in
 
         auto epilogue = [&](int e) {  // read chunk e's accumulators, finish the unit if it was its last chunk
             const int eb = e & 1;
@@ -454,6 +548,7 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
             // all take the same branch.
             if (ptx::named_bar_or(1, kStagers, *abort_flag != 0u)) break;
             if (reuse) {  // B (and its row scales) already hold this chunk
+                last_gc[buf] = gc;
                 ptx::mbar_arrive(bars + kBarBFull + 8 * buf);
                 if (gc >= 1) epilogue(gc - 1);
                 prev_item = cur.item;
@@ -469,6 +564,31 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
             const int n_items = m * n_words;
             const uint32_t bb = bbuf + (uint32_t)buf * kBBufStride;
             const uint32_t wbytes = 32u * (uint32_t)m;  // compact B: a block holds rows 0..2m-1
+            const uint32_t bfull = bars + kBarBFull + 8 * buf;
+            if (it.bsrc != nullptr) {
+                // prepared: the chunk's bytes in a few bulk copies that
+                // complete on BFull (its phase also waits for every staging
+                // thread's arrival below), and the chunk's row maxima
+                if (st_tid == 0) {
+                    const uint32_t bytes = (uint32_t)n_words * wbytes;
+                    const unsigned char *src = it.bsrc + (size_t)(k0 / 16) * wbytes;
+                    ptx::mbar_expect_tx(bfull, bytes);
+                    for (uint32_t o = 0; o < bytes; o += kBulkPiece)
+                        ptx::bulk_load(bb + o, src + o, min(kBulkPiece, bytes - o), bfull);
+                }
+                if (st_tid < m) xm[st_tid] = it.xmax[8 * cur.chunk + st_tid];
+                held_item[buf] = cur.item;
+                held_chunk[buf] = cur.chunk;
+                last_gc[buf] = gc;
+                ptx::mbar_arrive(bfull);
+                if (gc >= 1) epilogue(gc - 1);
+                prev_item = cur.item;
+                prev_tile = cur.tile;
+                prev_last = cur.last_chunk_of_unit();
+                ++gc;
+                ok = cur.next_chunk();
+                continue;
+            }
             if (st_tid < 8) xm[st_tid] = 0u;
             ptx::named_bar_sync(1, kStagers);
             // The compact layout keeps 32 bytes (hi and lo rows) per 16
@@ -505,8 +625,9 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
             }
             held_item[buf] = cur.item;
             held_chunk[buf] = cur.chunk;
+            last_gc[buf] = gc;
             ptx::fence_proxy_async_smem();  // my B writes -> visible to the tensor core
-            ptx::mbar_arrive(bars + kBarBFull + 8 * buf);
+            ptx::mbar_arrive(bfull);
             if (gc >= 1) epilogue(gc - 1);
             prev_item = cur.item;
             prev_tile = cur.tile;
@@ -515,6 +636,13 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
             ok = cur.next_chunk();
         }
         if (!ptx::named_bar_or(1, kStagers, *abort_flag != 0u) && gc >= 1) epilogue(gc - 1);
+        // After an abort a bulk copy into a B buffer may still be in flight:
+        // its buffer's last BFull phase completes only when it has landed
+        // (every staging thread has arrived on it).
+        if (st_tid == 0)
+            for (int b = 0; b < 2; ++b)
+                if (last_gc[b] >= 0)
+                    drain_wait(bars + kBarBFull + 8 * b, (uint32_t)(last_gc[b] >> 1) & 1u, &g_batched_error);
     }
 
     __syncthreads();
@@ -564,21 +692,58 @@ std::vector<int> plan_groups(const tern_batch_item *items, int n)
     return even.size() <= greedy.size() ? even : greedy;
 }
 
+// Workspace of prepared activations per (device, stream), grown on demand.
+// A grown-out buffer is never freed: a launch captured in a CUDA graph keeps
+// the address it was captured with.  Returns nullptr if the allocation fails
+// (the staging warps then build B themselves).
+void *workspace(cudaStream_t stream, size_t need)
+{
+    struct Buf {
+        void *p = nullptr;
+        size_t bytes = 0;
+    };
+    static std::mutex mu;
+    static std::map<std::pair<int, cudaStream_t>, Buf> all;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    std::lock_guard<std::mutex> lock(mu);
+    Buf &b = all[{dev, stream}];
+    if (b.bytes >= need) return b.p;
+    const size_t bytes = need > 2 * b.bytes ? need : 2 * b.bytes;
+    // an allocation is allowed while a stream of this thread is being captured
+    cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+    if (cudaThreadExchangeStreamCaptureMode(&mode) != cudaSuccess) return nullptr;
+    void *p = nullptr;
+    const cudaError_t e = cudaMalloc(&p, bytes);
+    cudaThreadExchangeStreamCaptureMode(&mode);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    b.p = p;
+    b.bytes = bytes;
+    return p;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
 }  // namespace
 
 int batched_launches(const tern_batch_item *items, int n)
 {
     int launches = 0, begin = 0;
     for (const int end : plan_groups(items, n)) {
-        bool any = false;
+        bool any = false, prep = false;
         for (int i = begin; i < end; ++i) {
             if (items[i].w->rows == 0) continue;
-            if (items[i].w->k == 0)
+            if (items[i].w->k == 0) {
                 ++launches;
-            else
+            } else {
                 any = true;
+                prep = prep || items[i].m >= 2;
+            }
         }
-        launches += any ? 1 : 0;
+        launches += (any ? 1 : 0) + (prep ? 1 : 0);
         begin = end;
     }
     return launches;
@@ -624,8 +789,11 @@ tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t strea
             it.m = b.m;
             it.swiglu = b.up != nullptr;
             it.stages = (it.k / 16 + kStageWords - 1) / kStageWords;
+            // chunks: the fewest that fit a B buffer, of equal stage counts
+            // (a short last chunk would pay the per-chunk costs for little work)
             const int cap = kBBufBytes / (1024 * it.m);  // stages of compact B one buffer holds
-            it.cstages = it.stages < cap ? it.stages : cap;
+            const int n_chunks = (it.stages + cap - 1) / cap;
+            it.cstages = (it.stages + n_chunks - 1) / n_chunks;
             it.unit0 = units;
             it.map = n_maps;
             const int tile_rows = it.swiglu ? 64 : 128;
@@ -640,6 +808,53 @@ tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t strea
         begin = end;
         if (cnt == 0) continue;
         prm.n_items = cnt;
+
+        // Items with m >= 2 take their B from the workspace, written by one
+        // k_tern_bprep launch just before: per item the padded K's words
+        // (1024m bytes per stage), then 8 row maxima per chunk.
+        PrepParams pp;
+        std::memset(&pp, 0, sizeof(pp));
+        size_t ws_need = 0;
+        std::vector<std::pair<size_t, size_t>> ws_off(cnt);
+        for (int j = 0; j < cnt; ++j) {
+            const Item &it = prm.item[j];
+            if (it.m < 2) continue;
+            const int n_chunks = (it.stages + it.cstages - 1) / it.cstages;
+            if (it.cstages * kStageWords > kPrepWords * kPrepThreads) return TERN_ERR_SHAPE;  // cannot happen: m >= 2
+            ws_off[j].first = ws_need;
+            ws_need += align256((size_t)it.stages * 1024u * (size_t)it.m);
+            ws_off[j].second = ws_need;
+            ws_need += align256((size_t)n_chunks * 8u * sizeof(uint32_t));
+        }
+        unsigned char *ws = ws_need > 0 ? static_cast<unsigned char *>(workspace(stream, ws_need)) : nullptr;
+        if (ws != nullptr) {
+            for (int j = 0; j < cnt; ++j) {
+                Item &it = prm.item[j];
+                if (it.m < 2) continue;
+                it.bsrc = ws + ws_off[j].first;
+                it.xmax = reinterpret_cast<const uint32_t *>(ws + ws_off[j].second);
+                PrepItem &q = pp.item[pp.n_items++];
+                q.x = it.x;
+                q.b = ws + ws_off[j].first;
+                q.xmax = reinterpret_cast<uint32_t *>(ws + ws_off[j].second);
+                q.k = it.k;
+                q.m = it.m;
+                q.stages = it.stages;
+                q.cstages = it.cstages;
+                q.task0 = pp.n_tasks;
+                pp.n_tasks += (it.stages + it.cstages - 1) / it.cstages * it.m;
+            }
+            cudaLaunchConfig_t pcfg = {};
+            pcfg.gridDim = dim3((unsigned)pp.n_tasks, 1, 1);
+            pcfg.blockDim = dim3(kPrepThreads, 1, 1);
+            pcfg.stream = stream;
+            cudaLaunchAttribute pattr;
+            pattr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            pattr.val.programmaticStreamSerializationAllowed = 1;
+            pcfg.attrs = &pattr;
+            pcfg.numAttrs = 1;
+            if (cudaLaunchKernelEx(&pcfg, k_tern_bprep, pp) != cudaSuccess) return TERN_ERR_CUDA;
+        }
         // contiguous runs of units with balanced stage counts
         const int ctas = units < sms ? units : (sms < kMaxCtas ? sms : kMaxCtas);
         long long total = 0;
@@ -653,6 +868,10 @@ tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t strea
             prm.unit_start[b] = u;
         }
         prm.unit_start[ctas] = units;
+        for (int b = 0, j = 0; b < ctas; ++b) {
+            while (j + 1 < cnt && prm.item[j + 1].unit0 <= prm.unit_start[b]) ++j;
+            prm.item_start[b] = j;
+        }
         for (int b = 0; b < ctas; ++b) {
             long long st = 0;
             for (int q = prm.unit_start[b]; q < prm.unit_start[b + 1]; ++q) st += unit_cost[q];

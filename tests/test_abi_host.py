@@ -154,12 +154,14 @@ def test_device_entry_points_reject_before_launch(lib):
 
 def test_batched_launch_plan(lib):
     """Launch count of tern_gemm_batched: 128 items or 144 weight matrices per
-    launch, k == 0 items on a launch of their own, rows == 0 items on none."""
+    launch, k == 0 items on a launch of their own, rows == 0 items on none, and
+    one activation-preparing launch per group that holds an item with m >= 2."""
     keep = []
 
     def arr(spec):
         a = (tern.CBatchItem * len(spec))()
-        for i, (rows, k, sw) in enumerate(spec):
+        for i, sp in enumerate(spec):
+            rows, k, sw = sp[:3]
             w = _mat(rows, k)
             keep.append(w)
             a[i].w = ctypes.addressof(w)
@@ -167,13 +169,15 @@ def test_batched_launch_plan(lib):
                 u = _mat(rows, k)
                 keep.append(u)
                 a[i].up = ctypes.addressof(u)
-            a[i].x, a[i].y, a[i].m = 0x3000, 0x4000, 1
+            a[i].x, a[i].y, a[i].m = 0x3000, 0x4000, sp[3] if len(sp) > 3 else 1
         return a
 
     cases = [([(4096, 4096, 0)] * 128, 1), ([(4096, 4096, 0)] * 129, 2), ([(64, 4096, 1)] * 72, 1),
              ([(64, 4096, 1)] * 73, 2), ([(0, 64, 0)] * 5, 0), ([(4, 0, 0)] * 3, 3),
              ([(4, 0, 0), (4096, 4096, 0), (0, 4, 0)], 2), ([(4096, 4096, 0)] * 252, 2),
-             ([(4096, 4096, 0)] * 257, 3), ([(4096, 4096, 0)] * 100 + [(64, 4096, 1)] * 30, 2)]
+             ([(4096, 4096, 0)] * 257, 3), ([(4096, 4096, 0)] * 100 + [(64, 4096, 1)] * 30, 2),
+             ([(4096, 4096, 0, 7)], 2), ([(12288, 4096, 1, 7), (4096, 12288, 0, 7)] * 4, 2),
+             ([(4096, 4096, 0, 2)] + [(4096, 4096, 0)] * 200, 3), ([(4, 0, 0, 7), (0, 64, 0, 3)], 1)]
     for spec, want in cases:
         assert tern.tern_gemm_batched_launches(arr(spec)) == want, (len(spec), want)
     assert lib.tern_gemm_batched_launches(None, 0) == 0

@@ -298,7 +298,9 @@ def test_batched_exact_integers_and_many_items():
     rng = np.random.default_rng(405)
     made = [_item(rng, 128 + 64 * (i % 5), 4096 if i % 3 else 12288, 1 + (i % 8), swiglu=(i % 4 == 0), int_x=True)
             for i in range(150)]
-    assert tern.tern_gemm_batched_launches([mi[0] for mi in made]) == 2
+    # two persistent launches, each after an activation-preparing launch
+    # (both groups hold items with m >= 2)
+    assert tern.tern_gemm_batched_launches([mi[0] for mi in made]) == 4
     tern.tern_gemm_batched([mi[0] for mi in made])
     torch.cuda.synchronize()
     for i, (it, ref, full) in enumerate(made):
