@@ -63,6 +63,8 @@ extern "C" {
 #define TERN_MAX_X_BYTES 196608
 /* Largest activation row count of tern_gemm_smallm*. */
 #define TERN_MAX_M 8
+/* Size of the fixed scratch of tern_gemm_batched_noalloc (4 MiB). */
+#define TERN_NOALLOC_WS_BYTES 4194304
 
 typedef enum {
     TERN_OK = 0,
@@ -188,6 +190,28 @@ TERN_API tern_status tern_gemm_batched(const tern_batch_item *items, int32_t n, 
  * (-TERN_ERR_NULL).  Not an operation of the model pages: a planning aid for
  * callers that count or capture launches. */
 TERN_API int32_t tern_gemm_batched_launches(const tern_batch_item *items, int32_t n);
+
+/* tern_gemm_batched for callers that must not allocate device memory: code
+ * running inside a memory budget that another allocator owns (a serving
+ * engine that reserves the GPU's memory for its caches up front, where a
+ * cudaMalloc from the library may fail or fragment that pool), and code
+ * that may not call cudaMalloc at all.  The model pages have no counterpart:
+ * the operation, items, checks, launches and results are those of
+ * tern_gemm_batched, byte for byte.  The difference is where the prepared
+ * activations of items with m >= 2 live: a module-scope device array of
+ * TERN_NOALLOC_WS_BYTES, set up by the CUDA runtime with the library's
+ * kernels, instead of the per-stream workspace.
+ * Limit: every launch group's prepared activations (about m * k * 2 bytes per
+ * item with m >= 2, k padded to a multiple of 512) must fit the array; a batch
+ * that needs more gets TERN_ERR_SHAPE before anything is launched.
+ * The first call on a device looks the array's address up
+ * (cudaGetSymbolAddress, with that device current; TERN_ERR_CUDA if that
+ * fails); make it before capturing a stream.  Nothing in the array must
+ * start at zero: each launch writes every byte it reads.  There is one
+ * array per device, shared by every stream: calls whose launches overlap in
+ * time (on different streams, or a captured graph replayed beside another
+ * call) race on it. */
+TERN_API tern_status tern_gemm_batched_noalloc(const tern_batch_item *items, int32_t n, void *stream);
 
 /* Synchronise `stream`, then report and clear the device error word that
  * bounded device-side waits set when they run out (TERN_ERR_TIMEOUT), or a

@@ -33,10 +33,12 @@ TERN_ERR_TIMEOUT = 8
 TERN_ERR_VALUE = 9
 TERN_MAX_X_BYTES = 196608
 TERN_MAX_M = 8
+TERN_NOALLOC_WS_BYTES = 4194304
 
 ABI_FUNCTIONS = (
     "tern_pack", "tern_validate", "tern_unpack", "tern_gemv", "tern_gemv_swiglu",
     "tern_gemm_smallm", "tern_gemm_smallm_swiglu", "tern_gemm_batched", "tern_gemm_batched_launches",
+    "tern_gemm_batched_noalloc",
     "tern_last_device_error",
     "tern_status_str", "tern_abi_version",
 )
@@ -84,6 +86,7 @@ def load(path: str | None = None):
             "tern_gemm_smallm_swiglu": [vp, vp, vp, i32, vp, vp],
             "tern_gemm_batched": [vp, i32, vp],
             "tern_gemm_batched_launches": [vp, i32],
+            "tern_gemm_batched_noalloc": [vp, i32, vp],
             "tern_last_device_error": [vp],
             "tern_status_str": [ctypes.c_int],
             "tern_abi_version": [],
@@ -225,6 +228,14 @@ def tern_gemm_batched(items, stream=None):
     arr = items if isinstance(items, ctypes.Array) else batch_items(items)
     _check(load().tern_gemm_batched(ctypes.cast(arr, ctypes.c_void_p) if len(arr) else None, len(arr),
                                     _stream_handle(stream)), "tern_gemm_batched")
+
+
+def tern_gemm_batched_noalloc(items, stream=None):
+    """tern_gemm_batched with its scratch in a fixed module-scope array of
+    TERN_NOALLOC_WS_BYTES instead of a library-allocated workspace."""
+    arr = items if isinstance(items, ctypes.Array) else batch_items(items)
+    _check(load().tern_gemm_batched_noalloc(ctypes.cast(arr, ctypes.c_void_p) if len(arr) else None, len(arr),
+                                            _stream_handle(stream)), "tern_gemm_batched_noalloc")
 
 
 def tern_gemm_batched_launches(items) -> int:

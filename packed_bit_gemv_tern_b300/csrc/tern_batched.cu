@@ -727,6 +727,29 @@ void *workspace(cudaStream_t stream, size_t need)
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
+// 512-code stages over K, and stages per chunk: the fewest chunks that fit a
+// B buffer, of equal stage counts (a short last chunk would pay the
+// per-chunk costs for little work).
+void chunk_plan(int k, int m, int &stages, int &cstages)
+{
+    stages = (k / 16 + kStageWords - 1) / kStageWords;
+    const int cap = kBBufBytes / (1024 * m);  // stages of compact B one buffer holds
+    const int n_chunks = (stages + cap - 1) / cap;
+    cstages = (stages + n_chunks - 1) / n_chunks;
+}
+
+// Workspace bytes of one prepared item (see Item::bsrc, Item::xmax).
+size_t prep_bytes(int stages, int cstages, int m)
+{
+    const int n_chunks = (stages + cstages - 1) / cstages;
+    return align256((size_t)stages * 1024u * (size_t)m) + align256((size_t)n_chunks * 8u * sizeof(uint32_t));
+}
+
+// Scratch of tern_gemm_batched_noalloc: module-scope device memory, which the
+// CUDA runtime sets up when it loads the library's kernels on a device, so
+// the entry point itself never allocates.
+__device__ __align__(256) unsigned char g_noalloc_ws[TERN_NOALLOC_WS_BYTES];
+
 }  // namespace
 
 int batched_launches(const tern_batch_item *items, int n)
@@ -749,7 +772,11 @@ int batched_launches(const tern_batch_item *items, int n)
     return launches;
 }
 
-tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t stream)
+namespace {
+
+// Launches the batch.  fixed_ws: a workspace the caller guarantees to be
+// large enough for every launch group (nullptr: the per-stream workspace).
+tern_status run_batched(const tern_batch_item *items, int n, cudaStream_t stream, unsigned char *fixed_ws)
 {
     static_assert(sizeof(Params) + sizeof(Maps) < 32000, "kernel parameters exceed 32 KB");
     const int sms = sm_count();
@@ -788,12 +815,7 @@ tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t strea
             it.k = b.w->k;
             it.m = b.m;
             it.swiglu = b.up != nullptr;
-            it.stages = (it.k / 16 + kStageWords - 1) / kStageWords;
-            // chunks: the fewest that fit a B buffer, of equal stage counts
-            // (a short last chunk would pay the per-chunk costs for little work)
-            const int cap = kBBufBytes / (1024 * it.m);  // stages of compact B one buffer holds
-            const int n_chunks = (it.stages + cap - 1) / cap;
-            it.cstages = (it.stages + n_chunks - 1) / n_chunks;
+            chunk_plan(it.k, it.m, it.stages, it.cstages);
             it.unit0 = units;
             it.map = n_maps;
             const int tile_rows = it.swiglu ? 64 : 128;
@@ -822,11 +844,11 @@ tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t strea
             const int n_chunks = (it.stages + it.cstages - 1) / it.cstages;
             if (it.cstages * kStageWords > kPrepWords * kPrepThreads) return TERN_ERR_SHAPE;  // cannot happen: m >= 2
             ws_off[j].first = ws_need;
-            ws_need += align256((size_t)it.stages * 1024u * (size_t)it.m);
-            ws_off[j].second = ws_need;
-            ws_need += align256((size_t)n_chunks * 8u * sizeof(uint32_t));
+            ws_off[j].second = ws_need + align256((size_t)it.stages * 1024u * (size_t)it.m);
+            ws_need += prep_bytes(it.stages, it.cstages, it.m);
         }
-        unsigned char *ws = ws_need > 0 ? static_cast<unsigned char *>(workspace(stream, ws_need)) : nullptr;
+        unsigned char *ws = nullptr;
+        if (ws_need > 0) ws = fixed_ws != nullptr ? fixed_ws : static_cast<unsigned char *>(workspace(stream, ws_need));
         if (ws != nullptr) {
             for (int j = 0; j < cnt; ++j) {
                 Item &it = prm.item[j];
@@ -892,6 +914,47 @@ tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t strea
         if (cudaGetLastError() != cudaSuccess) return TERN_ERR_CUDA;
     }
     return TERN_OK;
+}
+
+}  // namespace
+
+tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t stream)
+{
+    return run_batched(items, n, stream, nullptr);
+}
+
+tern_status gemm_batched_noalloc(const tern_batch_item *items, int n, cudaStream_t stream)
+{
+    // every launch group's prepared activations must fit the static scratch
+    // (the groups run one after another on the stream and reuse it)
+    int begin = 0;
+    for (const int end : plan_groups(items, n)) {
+        size_t need = 0;
+        for (int i = begin; i < end; ++i) {
+            const tern_batch_item &b = items[i];
+            if (b.w->rows == 0 || b.w->k == 0 || b.m < 2) continue;
+            int stages = 0, cstages = 0;
+            chunk_plan(b.w->k, b.m, stages, cstages);
+            need += prep_bytes(stages, cstages, b.m);
+        }
+        if (need > (size_t)TERN_NOALLOC_WS_BYTES) return TERN_ERR_SHAPE;
+        begin = end;
+    }
+    // the scratch's device address, looked up once per device
+    static std::mutex mu;
+    static void *addr[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TERN_ERR_CUDA;
+    void *ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (addr[dev] == nullptr && cudaGetSymbolAddress(&addr[dev], g_noalloc_ws) != cudaSuccess) {
+            addr[dev] = nullptr;
+            return TERN_ERR_CUDA;
+        }
+        ws = addr[dev];
+    }
+    return run_batched(items, n, stream, static_cast<unsigned char *>(ws));
 }
 
 tern_status take_batched_error()

@@ -319,22 +319,32 @@ extern "C" tern_status tern_gemm_smallm_swiglu(const tern_matrix *gate, const te
     return swiglu_dispatch(gate, up, x, m, h, (cudaStream_t)stream);
 }
 
-extern "C" tern_status tern_gemm_batched(const tern_batch_item *items, int32_t n, void *stream)
+// Checks every item of a batch as the single calls do.
+static tern_status check_batch(const tern_batch_item *items, int32_t n)
 {
     if (n < 0) return TERN_ERR_SHAPE;
     if (n == 0) return TERN_OK;
     if (items == nullptr) return TERN_ERR_NULL;
     for (int32_t i = 0; i < n; ++i) {
         const tern_batch_item &b = items[i];
-        if (b.up == nullptr) {
-            const tern_status st = check_gemm_args(b.w, nullptr, b.x, b.m, b.y);
-            if (st != TERN_OK) return st;
-        } else {
-            const tern_status st = check_gemm_args(b.w, b.up, b.x, b.m, b.y);
-            if (st != TERN_OK) return st;
-        }
+        const tern_status st = check_gemm_args(b.w, b.up, b.x, b.m, b.y);
+        if (st != TERN_OK) return st;
     }
+    return TERN_OK;
+}
+
+extern "C" tern_status tern_gemm_batched(const tern_batch_item *items, int32_t n, void *stream)
+{
+    const tern_status st = check_batch(items, n);
+    if (st != TERN_OK || n == 0) return st;
     return batched_dispatch(items, n, (cudaStream_t)stream);
+}
+
+extern "C" tern_status tern_gemm_batched_noalloc(const tern_batch_item *items, int32_t n, void *stream)
+{
+    const tern_status st = check_batch(items, n);
+    if (st != TERN_OK || n == 0) return st;
+    return gemm_batched_noalloc(items, n, (cudaStream_t)stream);
 }
 
 extern "C" int32_t tern_gemm_batched_launches(const tern_batch_item *items, int32_t n)

@@ -27,6 +27,10 @@ tern_status take_mma_error();
 // Number of kernel launches gemm_batched makes for these items (host only).
 int batched_launches(const tern_batch_item *items, int n);
 tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t s);
+// As gemm_batched, with the prepared activations in a fixed module-scope
+// scratch of TERN_NOALLOC_WS_BYTES (TERN_ERR_SHAPE, nothing launched, if a
+// launch group needs more).
+tern_status gemm_batched_noalloc(const tern_batch_item *items, int n, cudaStream_t s);
 tern_status take_batched_error();
 
 // Shared argument checks (tern_cuda.cu).
