@@ -181,6 +181,21 @@ def ncu_traffic(workload: str):
 # ---------------------------------------------------------------------------
 # CPU oracle baseline
 # ---------------------------------------------------------------------------
+def persistent_launches(batch) -> int:
+    """Launches of the persistent batched kernel for a batch: the launch count
+    of the same items with m = 1.  The launch groups do not depend on m; a
+    group that holds items with m >= 2 adds one short activation-preparing
+    launch, which the full count includes."""
+    import ctypes
+
+    import packed_bit_gemv_tern_b300 as tern
+    arr = (tern.CBatchItem * len(batch))()
+    ctypes.memmove(arr, batch, ctypes.sizeof(arr))
+    for it in arr:
+        it.m = 1
+    return tern.tern_gemm_batched_launches(arr)
+
+
 def oracle_sample_rate(wl, budget_s: float, threads: int):
     """Time the fp64 oracle over a bounded sample of the workload's calls.
 
@@ -311,6 +326,9 @@ def run_ours(args, dist: Dist):
 
     batch = workloads.batch_of(wl.calls) if args.api == "batched" else None
     launches_per_step = tern.tern_gemm_batched_launches(batch) if batch is not None else ncalls
+    # the dominant kernel's launches: the persistent kernel's (batched), or every call's
+    main_launches = persistent_launches(batch) if batch is not None else ncalls
+    prep_launches = launches_per_step - main_launches
 
     def step_fn():
         if batch is not None:
@@ -360,8 +378,10 @@ def run_ours(args, dist: Dist):
     step_ms = ms_max / args.steps
     value = dist.world * packed * args.steps / (ms_max * 1e-3) / 1e9
     us_per_call = 1e3 * step_ms / ncalls
-    per_launch_s = ms * 1e-3 / (args.steps * launches_per_step)
-    achieved = (alg / launches_per_step) / per_launch_s / 1e9
+    # the step's time over the dominant kernel's launches: with a preparing
+    # launch in the step, its (mostly overlapped) time is charged to them
+    per_launch_s = ms * 1e-3 / (args.steps * main_launches)
+    achieved = (alg / main_launches) / per_launch_s / 1e9
     peak, peak_kind = peaks()
     traffic, traffic_kernel = ncu_traffic(args.workload)
 
@@ -385,13 +405,16 @@ def run_ours(args, dist: Dist):
                    "algorithmic_bytes_per_step": alg, "us_per_call": round(us_per_call, 4),
                    "l2": "inputs larger than L2: each step streams %.0f MB of distinct buffers" % (packed / 1e6),
                    "graph": "one CUDA graph per step, replayed", "parallelism": f"replicas x{dist.world}",
-                   "api": (f"tern_gemm_batched: {launches_per_step} persistent launch(es) per step"
+                   "api": (f"tern_gemm_batched: {main_launches} persistent launch(es) per step"
+                           + (f" and {prep_launches} activation-preparing launch(es)" if prep_launches else "")
                            if args.api == "batched" else "one tern_* launch per call")},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
                      "traffic": traffic, "traffic_kernel": traffic_kernel,
-                     "bytes_per_launch": alg // launches_per_step},
+                     "bytes_per_launch": alg // main_launches,
+                     "duration": ("CUDA-event step time / persistent launches per step"
+                                  + (" (includes the activation-preparing launch)" if prep_launches else ""))},
         "clocks": clk,
         "gpu_launches": args.steps * launches_per_step,
         "e2e": e2e,

@@ -56,3 +56,24 @@ def test_single_rank_needs_no_group():
     if d.world == 1:
         d.barrier()
         assert d.max(2.0) == 2.0
+
+
+def test_persistent_launch_count():
+    """bench.py's roofline divides by the persistent kernel's launches only:
+    a group with m >= 2 items adds a preparing launch to the full count."""
+    import ctypes
+
+    sys.path.insert(0, ROOT)
+    import bench
+    import packed_bit_gemv_tern_b300 as tern
+    from packed_bit_gemv_tern_b300 import build
+    build.build()
+    tern.load()
+    w = tern.CMatrix(4096, 4096, 0x1000, 0x2000, None)
+    for m, n, total, main in ((1, 100, 1, 1), (7, 8, 2, 1), (7, 200, 4, 2), (2, 1, 2, 1)):
+        arr = (tern.CBatchItem * n)()
+        for i in range(n):
+            arr[i].w, arr[i].x, arr[i].y, arr[i].m = ctypes.addressof(w), 0x3000, 0x4000, m
+        assert tern.tern_gemm_batched_launches(arr) == total
+        assert bench.persistent_launches(arr) == main
+        assert [it.m for it in arr] == [m] * n  # the caller's array is untouched
