@@ -220,14 +220,26 @@ def test_side_stream_and_reuse():
     _close(y.cpu().numpy(), oracle.gemm(codes, scale, k, xb, threads=THREADS), "side stream")
 
 
-@pytest.mark.parametrize("name", ["c0", "c1", "c2", "c3"])
-def test_bench_workloads_full_size(name):
-    """The benchmark's own workloads at full size, in the launch configuration
-    it times (one step issued through run_calls); every distinct matrix
-    checked against the oracle element by element."""
-    wl = workloads.build(name, rotate_bytes=1, distinct=1)
-    workloads.run_calls(wl.calls)
+def _run_step(wl, api):
+    """One step of a workload: through tern_gemm_batched as bench.py times it by
+    default (one persistent launch per group, after an activation-preparing
+    launch when items have m >= 2), or one tern_* call per linear."""
+    if api == "batched":
+        workloads.run_batched(workloads.batch_of(wl.calls))
+    else:
+        workloads.run_calls(wl.calls)
     torch.cuda.synchronize()
+    assert tern.tern_last_device_error() == tern.TERN_OK
+
+
+@pytest.mark.parametrize("api", ["batched", "calls"])
+@pytest.mark.parametrize("name", ["c0", "c1", "c2", "c3"])
+def test_bench_workloads_full_size(name, api):
+    """The benchmark's own workloads at full size, in both launch
+    configurations bench.py can time; every distinct matrix checked against
+    the oracle element by element."""
+    wl = workloads.build(name, rotate_bytes=1, distinct=1)
+    _run_step(wl, api)
     for c, h in zip(wl.calls, wl.host):
         lin = h["lin"]
         codes = oracle.pack(lin.t)
@@ -240,12 +252,12 @@ def test_bench_workloads_full_size(name):
         _close(c.y.cpu().numpy(), ref, f"{name}:{c.name}")
 
 
-def test_sweep_sampled_rows():
+@pytest.mark.parametrize("api", ["batched", "calls"])
+def test_sweep_sampled_rows(api):
     """Two layers of the 36-layer sweep (all seven shapes, the layer-1 code
     mix), sampled rows of every linear against the oracle."""
     wl = workloads.build("c4", layers=2)
-    workloads.run_calls(wl.calls)
-    torch.cuda.synchronize()
+    _run_step(wl, api)
     rng = np.random.default_rng(0)
     for c, h in zip(wl.calls, wl.host):
         lin = h["lin"]
