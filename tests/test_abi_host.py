@@ -41,6 +41,21 @@ def test_exports_every_declared_symbol(lib):
     assert tern.tern_abi_version() == 1
 
 
+def test_header_constants_match_binding():
+    """Every TERN_* integer constant of include/tern.h has the same value in
+    the Python binding."""
+    src = open(os.path.join(ROOT, "include", "tern.h")).read()
+    defs = dict(re.findall(r"^#define\s+(TERN_\w+)\s+(\d+)\s*$", src, flags=re.M))
+    enums = dict(re.findall(r"\b(TERN_\w+)\s*=\s*(\d+)", src))
+    both = {**defs, **enums}
+    assert "TERN_NOALLOC_WS_BYTES" in both and "TERN_MAX_X_BYTES" in both
+    for name, val in both.items():
+        if hasattr(tern, name):
+            assert getattr(tern, name) == int(val), name
+    for name in ("TERN_NOALLOC_WS_BYTES", "TERN_MAX_X_BYTES", "TERN_MAX_M", "TERN_ERR_TIMEOUT"):
+        assert hasattr(tern, name), name
+
+
 def test_status_strings(lib):
     for s in range(10):
         assert tern.tern_status_str(s)
