@@ -181,6 +181,38 @@ def ncu_traffic(workload: str):
 # ---------------------------------------------------------------------------
 # CPU oracle baseline
 # ---------------------------------------------------------------------------
+def step_spread(graph, stream, n: int, ncalls: int) -> dict:
+    """Spread of the per-call time: a second pass of n steps after the timed
+    region, each step between its own CUDA events (so consecutive steps do not
+    overlap here, unlike in the timed region); p10, median and p90 of the step
+    time divided by the calls per step.  Never fails the bench line."""
+    try:
+        import torch
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        with torch.cuda.stream(stream):
+            for a, b in evs:
+                a.record(stream)
+                graph.replay()
+                b.record(stream)
+        stream.synchronize()
+        out = spread_stats([1e3 * a.elapsed_time(b) / ncalls for a, b in evs])
+        out["how"] = "each step between its own CUDA events, after the timed region"
+        return out
+    except Exception as e:  # the spread is informative only
+        return {"error": f"{type(e).__name__}: {e}"}
+
+
+def spread_stats(us_per_call) -> dict:
+    """p10, median and p90 (nearest rank) of per-call times in µs."""
+    per = sorted(us_per_call)
+
+    def pct(q):
+        return round(per[min(len(per) - 1, int(q * (len(per) - 1) + 0.5))], 4)
+
+    return {"steps": len(per), "us_per_call_p10": pct(0.1), "us_per_call_median": pct(0.5),
+            "us_per_call_p90": pct(0.9)}
+
+
 def persistent_launches(batch) -> int:
     """Launches of the persistent batched kernel for a batch: the launch count
     of the same items with m = 1.  The launch groups do not depend on m; a
@@ -372,6 +404,7 @@ def run_ours(args, dist: Dist):
     ms_max = dist.max(ms)
     if tern.tern_last_device_error(stream) != tern.TERN_OK:
         raise SystemExit("device error during the timed region")
+    spread = step_spread(graph, stream, min(args.steps, 200), ncalls)
 
     packed = wl.packed_bytes
     alg = wl.algorithmic_bytes
@@ -405,6 +438,7 @@ def run_ours(args, dist: Dist):
                    "algorithmic_bytes_per_step": alg, "us_per_call": round(us_per_call, 4),
                    "l2": "inputs larger than L2: each step streams %.0f MB of distinct buffers" % (packed / 1e6),
                    "graph": "one CUDA graph per step, replayed", "parallelism": f"replicas x{dist.world}",
+                   "gpu": torch.cuda.get_device_name(dev), "spread": spread,
                    "api": (f"tern_gemm_batched: {main_launches} persistent launch(es) per step"
                            + (f" and {prep_launches} activation-preparing launch(es)" if prep_launches else "")
                            if args.api == "batched" else "one tern_* launch per call")},

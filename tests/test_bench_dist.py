@@ -98,3 +98,20 @@ def test_reference_arm_prints_one_json_line():
     assert d["impl"] == "reference" and d["value"] > 0 and d["steps"] == 2
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_step_spread_helpers():
+    """The per-call spread: nearest-rank percentiles, and a failure inside the
+    spread pass (here: no GPU) is reported in the line, never raised."""
+    sys.path.insert(0, ROOT)
+    import bench
+    st = bench.spread_stats([float(v) for v in range(101, 0, -1)])  # 1..101 in any order
+    assert (st["steps"], st["us_per_call_p10"], st["us_per_call_median"], st["us_per_call_p90"]) == (101, 11.0, 51.0, 91.0)
+    assert bench.spread_stats([2.5])["us_per_call_median"] == 2.5
+
+    class NoGraph:
+        def replay(self):
+            raise RuntimeError("no graph")
+
+    out = bench.step_spread(NoGraph(), None, 3, 1)
+    assert set(out) == {"error"}
