@@ -215,17 +215,21 @@ def spread_stats(us_per_call) -> dict:
 
 def persistent_launches(batch) -> int:
     """Launches of the persistent batched kernel for a batch: the launch count
-    of the same items with m = 1.  The launch groups do not depend on m; a
-    group that holds items with m >= 2 adds one short activation-preparing
-    launch, which the full count includes."""
+    of the same items with m = 1, less the small launch of each item with
+    rows > 0 and k == 0.  The launch groups do not depend on m; a group that
+    holds items with m >= 2 adds one short activation-preparing launch, which
+    the full count includes."""
     import ctypes
 
     import packed_bit_gemv_tern_b300 as tern
     arr = (tern.CBatchItem * len(batch))()
     ctypes.memmove(arr, batch, ctypes.sizeof(arr))
+    k_zero = 0
     for it in arr:
         it.m = 1
-    return tern.tern_gemm_batched_launches(arr)
+        w = tern.CMatrix.from_address(it.w)
+        k_zero += 1 if w.rows > 0 and w.k == 0 else 0
+    return tern.tern_gemm_batched_launches(arr) - k_zero
 
 
 def oracle_sample_rate(wl, budget_s: float, threads: int):

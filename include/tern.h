@@ -1,11 +1,11 @@
 /*
  * tern.h -- C ABI of the B300 ternary packed-weight linear layer.
  *
- * The operation (Neutrino-1 8B model page, intro: "every one of its 252
- * transformer linears is stored in a ternary-family weight format ... the
- * weights stay bit-packed at rest and are decoded inside the matrix kernels";
- * "Where the bytes live": per-row metadata of row dimensions, scales and row
- * sums) is, for one projection with R output rows and K inputs,
+ * The operation (Neutrino-1 8B model page: the intro states that all 252
+ * transformer linears use a ternary-family weight format kept bit-packed in
+ * memory and decoded by the matrix kernels themselves; "Where the bytes
+ * live" lists per-row metadata of row dimensions, scales and row sums) is,
+ * for one projection with R output rows and K inputs,
  *
  *     y[m][r] = scale[r] * sum_{k < K} t[r][k] * x[m][k],   t[r][k] in {-1,0,+1}
  *
@@ -27,11 +27,35 @@
  *     checks; the GEMV kernels do not read it).
  *
  * Activations x are bf16, passed as their uint16 bit patterns, row-major
- * [M][K] (M = 1 for the GEMV).  Outputs are fp32, row-major [M][R].
+ * [M][K] (M = 1 for the GEMV), finite.  Outputs are fp32, row-major [M][R].
+ *
+ * Arithmetic.  The kernels decode each code to an e4m3 weight of exactly
+ * 0 or +-2 and multiply on the tensor cores with fp32 accumulation.  Each
+ * activation row enters as e4m3 terms under power-of-two scales, per row
+ * and per K range a kernel stages at once (a chunk): x = (hi + lo/16) * 2^-s
+ * with hi, lo e4m3, which is exact for every element at least 2^-13 of the
+ * row's maximum (2^e <= max|x| < 2^(e+1)) and off by at most 2^(e-21)
+ * below that.  When those smaller elements could move the row's sum by more
+ * than 2^-24 of sum|x| (n_small * 2^(e-21) > 2^-24 * sum|x|: outlier
+ * channels), the chunk is taken in two bands instead: band A holds the
+ * elements within 2^13 of the maximum, band B the others under a scale of
+ * their own (2^f <= band-B max < 2^(f+1)), exact down to 2^-13 of it and
+ * off by at most 2^(f-21) below.  Within a band the sums are fp32; bands,
+ * chunks and split-K ranks are added as exact fp32 pairs (TwoSum) and
+ * rounded once.
  *
  * Conventions for every entry point:
- *   - The caller owns every buffer; the library allocates no device memory
- *     on any call and keeps no pointer after a call returns.
+ *   - The caller owns every buffer it passes.  Device memory the library
+ *     holds itself: one error word per kernel family and the
+ *     TERN_NOALLOC_WS_BYTES array of tern_gemm_batched_noalloc (both
+ *     module-scope, set up when the library's kernels are loaded on a
+ *     device), and the workspace tern_gemm_batched allocates on first need
+ *     (see there).  tern_gemv, tern_gemv_swiglu, tern_gemm_smallm*,
+ *     tern_unpack and tern_gemm_batched_noalloc never allocate.
+ *   - Encoded TMA descriptors of weight matrices are cached on the host by
+ *     (codes pointer, shape); a descriptor holds only that address and
+ *     shape, so a later matrix at the same address with the same shape
+ *     reuses it correctly.
  *   - Device entry points are asynchronous on the caller's stream
  *     (a cudaStream_t passed as void*; NULL is the legacy default stream).
  *     Arguments are checked on the host before anything is launched; a
@@ -116,7 +140,7 @@ TERN_API tern_status tern_validate(const uint32_t *codes, int32_t rows, int32_t 
 /* ---------------------------------------------------------------------- */
 
 /* Decode a packed matrix to int8 t_out [rows][k] (debug / exactness gate;
- * "decoded inside the matrix kernels" made visible).  t_out: 16-byte aligned.
+ * the in-kernel decode made visible).  t_out: 16-byte aligned.
  * The invalid pattern decodes to -2. */
 TERN_API tern_status tern_unpack(const tern_matrix *w, int8_t *t_out, void *stream);
 
@@ -171,14 +195,15 @@ typedef struct {
  * Workspace: when a launch group holds items with m >= 2, a short kernel
  * runs just before it and writes those items' activations, split into the
  * operand form the tensor cores read, to a device workspace that the library
- * owns: one per (device, stream), allocated with cudaMalloc on first need
+ * owns: one per (context, stream), allocated with cudaMalloc on first need
  * (also while the stream is being captured), grown by doubling and never
  * freed, since a captured launch keeps its address.  Launches on one stream
  * are ordered, so they share it safely; a captured graph must not run at the
  * same time as other calls on the stream it was captured on.  If the
- * allocation fails, the persistent kernel builds the operand itself (slower,
- * same results).  n == 0 is a no-op; items == NULL gives TERN_ERR_NULL,
- * n < 0 TERN_ERR_SHAPE. */
+ * allocation fails the call returns TERN_ERR_CUDA (launch groups before the
+ * failing one have been launched); tern_gemm_batched_noalloc needs no
+ * allocation.  n == 0 is a no-op; items == NULL gives TERN_ERR_NULL, n < 0
+ * TERN_ERR_SHAPE. */
 TERN_API tern_status tern_gemm_batched(const tern_batch_item *items, int32_t n, void *stream);
 
 /* Number of kernel launches tern_gemm_batched makes for these items (host
@@ -201,22 +226,38 @@ TERN_API int32_t tern_gemm_batched_launches(const tern_batch_item *items, int32_
  * activations of items with m >= 2 live: a module-scope device array of
  * TERN_NOALLOC_WS_BYTES, set up by the CUDA runtime with the library's
  * kernels, instead of the per-stream workspace.
- * Limit: every launch group's prepared activations (about m * k * 2 bytes per
+ * Limit: every launch group's prepared activations (about m * k * 4 bytes per
  * item with m >= 2, k padded to a multiple of 512) must fit the array; a batch
  * that needs more gets TERN_ERR_SHAPE before anything is launched.
- * The first call on a device looks the array's address up
- * (cudaGetSymbolAddress, with that device current; TERN_ERR_CUDA if that
- * fails); make it before capturing a stream.  Nothing in the array must
- * start at zero: each launch writes every byte it reads.  There is one
- * array per device, shared by every stream: calls whose launches overlap in
- * time (on different streams, or a captured graph replayed beside another
- * call) race on it. */
+ * The array takes its device memory when the CUDA runtime loads the
+ * library's kernels on a device, which with lazy module loading (the
+ * default) is the first launch of this file's kernels there, possibly this
+ * call: make one warm-up call (n == 1, one small item) on each device
+ * before reserving the device's memory for other pools and before
+ * capturing a stream.  The first call in a context also looks the array's
+ * address up (cudaGetSymbolAddress, with that device current;
+ * TERN_ERR_CUDA if that fails); a context created after a device reset
+ * looks it up again.  Nothing in the array must start at zero: each launch
+ * writes every byte it reads.  There is one array per device, shared by
+ * every stream: calls whose launches overlap in time (on different
+ * streams, or a captured graph replayed beside another call) race on it. */
 TERN_API tern_status tern_gemm_batched_noalloc(const tern_batch_item *items, int32_t n, void *stream);
 
 /* Synchronise `stream`, then report and clear the device error word that
  * bounded device-side waits set when they run out (TERN_ERR_TIMEOUT), or a
  * pending CUDA error (TERN_ERR_CUDA).  TERN_OK otherwise. */
 TERN_API tern_status tern_last_device_error(void *stream);
+
+/* Bound of every device-side mbarrier wait of later launches, in SM clock
+ * cycles (default 2^31, about one second at the B300's maximum clock);
+ * cycles <= 0 restores the default.  A wait that runs out sets the device
+ * error word, and the kernel stops, waits (with the default bound) for its
+ * own copies and MMAs in flight, releases its tensor memory and returns, so
+ * the context stays usable and tern_last_device_error reports
+ * TERN_ERR_TIMEOUT.  Not an operation of the model pages: a diagnostic that
+ * lets a test make a wait run out.  Launches already made, and launches
+ * captured in a graph, keep the bound they were made with. */
+TERN_API void tern_set_wait_limit(int64_t cycles);
 
 /* Static description of a status code (never NULL). */
 TERN_API const char *tern_status_str(tern_status s);

@@ -39,7 +39,7 @@ ABI_FUNCTIONS = (
     "tern_pack", "tern_validate", "tern_unpack", "tern_gemv", "tern_gemv_swiglu",
     "tern_gemm_smallm", "tern_gemm_smallm_swiglu", "tern_gemm_batched", "tern_gemm_batched_launches",
     "tern_gemm_batched_noalloc",
-    "tern_last_device_error",
+    "tern_last_device_error", "tern_set_wait_limit",
     "tern_status_str", "tern_abi_version",
 )
 
@@ -88,6 +88,7 @@ def load(path: str | None = None):
             "tern_gemm_batched_launches": [vp, i32],
             "tern_gemm_batched_noalloc": [vp, i32, vp],
             "tern_last_device_error": [vp],
+            "tern_set_wait_limit": [ctypes.c_int64],
             "tern_status_str": [ctypes.c_int],
             "tern_abi_version": [],
         }
@@ -96,6 +97,7 @@ def load(path: str | None = None):
             f.argtypes = args
             f.restype = ctypes.c_int
         lib.tern_status_str.restype = ctypes.c_char_p
+        lib.tern_set_wait_limit.restype = None
         lib.tern_abi_version.restype = ctypes.c_int32
         _lib = lib
         return lib
@@ -249,6 +251,12 @@ def tern_gemm_batched_launches(items) -> int:
 
 def tern_last_device_error(stream=None) -> int:
     return int(load().tern_last_device_error(_stream_handle(stream)))
+
+
+def tern_set_wait_limit(cycles: int = 0):
+    """Bound of the kernels' device-side waits for later launches, in SM
+    cycles (0 restores the default); a diagnostic for the time-out path."""
+    load().tern_set_wait_limit(int(cycles))
 
 
 def tern_status_str(status: int) -> str:

@@ -7,12 +7,13 @@
 // a unit is one 128-row tile (64 gate + 64 up rows for a SwiGLU pair) of one
 // item over the item's whole K, so no unit needs a cross-CTA reduction.  The
 // host balances the runs by packed bytes.  K is processed in chunks of up to
-// 28672 / m codes (the whole K for m = 1 at every Neutrino shape); the B
-// operand (activations as two e4m3 terms under a per-row power-of-two scale
-// per chunk, see split_pair) and the fp32 accumulators are double buffered
-// per chunk, a chunk's B is reused by every later tile of the item on the
-// same buffer, and fetching the next chunk's B and reading the previous
-// chunk's sums overlap the weight stream.  Roles (17 warps):
+// 14336 / m codes (the whole K for m = 1 at every Neutrino shape); the B
+// operand (each activation as four e4m3 terms in two magnitude bands under
+// per-row power-of-two scales per chunk, see split_word2) and the fp32
+// accumulators are double buffered per chunk; a chunk's B is reused by every
+// later tile of the item on the same buffer, and fetching
+// the next chunk's B and reading the previous chunk's sums overlap the weight
+// stream.  Roles (17 warps):
 //   * warp 0, lane 0: TMA producer; streams every stage of every unit of the
 //     CTA through a 6-deep ring of 16 KB stages (128 rows x 512 codes,
 //     128-byte swizzle), never waiting on activations.
@@ -28,8 +29,10 @@
 //     chunk columns (128 codes of a row each) of the stages s = g (mod 3)
 //     into e4m3 +-2/0 bytes (decode8) in TMEM slot g, and lane 0 of warp q
 //     of the group then issues the K=32 steps of column q (tcgen05.mma
-//     kind::f8f6f4, A from TMEM, B from shared memory, M = 128, N = 16) into
-//     the column's accumulator of the chunk's buffer.  Three decoder warps
+//     kind::f8f6f4, A from TMEM, B from shared memory, M = 128) into the
+//     column's accumulator of the chunk's buffer: four columns of 128 codes
+//     at N = 16 (m <= 4), or two of 256 codes issued by warps 0 and 1 at
+//     N = 32 (m >= 5), so both fit the same 128 accumulator columns.  Three decoder warps
 //     per scheduler hide each other's barrier latency.
 // Every mbarrier wait is bounded; on time-out the kernel records the error,
 // stops, drains its copies and MMAs, releases its tensor memory and returns.
@@ -40,6 +43,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <set>
 #include <utility>
 #include <vector>
 
@@ -69,17 +73,19 @@ constexpr int kCols = 4;                   // chunk columns of a stage; warp q o
 constexpr int kDecGroups = 3;
 constexpr int kASlots = 3;                 // TMEM A slots, one stage (128 columns) each
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kDCol = kASlots * 128;  // D[buf][k] at kDCol + 16 * (kCols * buf + k)
-// B buffer of one chunk in the compact layout: the 2m rows (hi/lo of each
-// activation row) of a 16-code block are contiguous, blocks 32m bytes apart.
-// The MMA reads eight rows of a core matrix from each block start and eight
-// more 128 bytes on, so rows past 2m (ignored D columns) read neighbouring
-// blocks' bytes and the last block reads up to 256 bytes past its start.
+// Accumulators: 128 columns from kDCol, two buffers of 64 that alternate
+// chunk by chunk.  N = 16 (m <= 4): D[buf][q] at kDCol + 16 * (4 buf + q) for
+// the four 128-code columns q of a stage.  N = 32 (m >= 5): D[buf][q] at
+// kDCol + 32 * (2 buf + q) for two 256-code columns.
+constexpr uint32_t kDCol = kASlots * 128;
+// Two B buffers, contiguous, then the MMA's read slack.  A chunk is planned
+// so that its one-band operand (b_block_bytes(m, 1) per 16-code block) fits
+// one buffer; a chunk that needs two bands (twice the bytes) takes both
+// buffers, starting at the first.
 #ifndef TERN_BBUF_KB
 #define TERN_BBUF_KB 56
 #endif
 constexpr int kBBufBytes = TERN_BBUF_KB * 1024;
-constexpr int kBBufStride = kBBufBytes + 256;
 // Weight ring depth: 96 KB in flight per SM covers DRAM latency at the HBM
 // rate (a plain TMA stream of these stages runs as fast with 6 as with 9);
 // the rest of shared memory goes to the two 56 KB activation buffers.  The
@@ -99,16 +105,17 @@ struct Item {
     int cstages; // stages per K chunk (the last may be shorter); a chunk's B fits one buffer
     int unit0;   // first global unit of this item
     int map;     // its codes' tensor map (gate, then up, for a SwiGLU pair)
-    // B prepared by k_tern_bprep (nullptr: the staging warps build it): word
-    // w of row i of the item's padded K at byte w * 32m + 32i (hi row, then
-    // lo row), so chunk c is the contiguous range from c * cstages * 1024m;
-    // xmax[8c + i] = the row maximum (fp32 bits of |x|) over chunk c.
+    // B prepared by k_tern_bprep (m >= 2; nullptr for m = 1): the one-band
+    // compact layout of the padded K (word w of row i at w * 32m + 32i), so
+    // chunk c starts at byte c * cstages * 1024m; meta[kMetaWords * c ...]
+    // holds its rows' maxima and band-B flags.
     const unsigned char *bsrc;
-    const uint32_t *xmax;
+    const uint32_t *meta;
 };
 
 struct Params {
     int n_items;
+    long long wait_limit;          // bound of every Waiter, in cycles
     int unit_start[kMaxCtas + 1];  // CTA b runs units [unit_start[b], unit_start[b + 1])
     int item_start[kMaxCtas];      // the item holding unit unit_start[b]
     int stages_cta[kMaxCtas];      // 512-code stages in CTA b's run
@@ -122,7 +129,7 @@ struct Maps {
 // Shared-memory layout (bytes from the 1024-aligned base).
 constexpr uint32_t kOffW = 0;
 constexpr uint32_t kOffB = kOffW + kWStages * kStageBytes;
-constexpr uint32_t kOffXch = kOffB + 2 * kBBufStride;  // [64][8] fp32
+constexpr uint32_t kOffXch = kOffB + 2 * kBBufBytes + kBPad;  // [64][8] fp32
 constexpr uint32_t kOffBar = kOffXch + 64 * 8 * 4;
 constexpr uint32_t kBarWFull = 0;                       // [kWStages]
 constexpr uint32_t kBarWEmpty = kBarWFull + 8 * kWStages;
@@ -134,8 +141,13 @@ constexpr uint32_t kBarDEmpty = kBarDFull + 16;
 constexpr uint32_t kBarDrain = kBarDEmpty + 16;  // one commit per issuing warp on exit
 constexpr uint32_t kBarTurn = kBarDrain + 8;     // [kCols][kDecGroups]: group g's turn on column q
 constexpr uint32_t kWordsOff = kBarTurn + 8 * kCols * kDecGroups;
-// words: [0] tmem base, [1] abort, [8..15] xmax buffer 0, [16..23] xmax buffer 1
-constexpr uint32_t kSmemBytes = 1024 + kOffBar + kWordsOff + 32 * 4;
+// words: [0] tmem base, [1] abort, [8..31] B buffer 0's chunk metadata,
+// [32..55] buffer 1's: per activation row i, [2i] row maximum and [2i + 1]
+// band-B maximum; [16] the chunk's number times 4 plus its band count; [17],
+// [18] scratch of the m = 1 build
+constexpr uint32_t kWordsCount = 64;
+constexpr uint32_t kXmWords = 24;
+constexpr uint32_t kSmemBytes = 1024 + kOffBar + kWordsOff + kWordsCount * 4;
 
 __device__ unsigned int g_batched_error;
 
@@ -190,20 +202,27 @@ struct Cursor {
 
 // ------------------------------------------------------------------ B prep
 // One CTA per (item, chunk, activation row) of the items with m >= 2: the
-// row's largest |x| over the chunk, then every word (16 k) of the chunk split
-// into its hi and lo e4m3 rows at the row's scale (split_word), written in
-// the compact layout the MMA reads (Item::bsrc).  Words past K are zeros.
-// The result is the same, byte for byte, as the staging warps' own build.
-// A chunk holds at most 28 stages (m = 2), so each thread keeps its words in
-// registers between the two passes and all loads are in flight at once.
+// row's largest |x| over the chunk; below the band threshold it sets, the
+// largest |x| (band B), the count of nonzero elements and the sum of all
+// |x|, and from these whether the row needs band B (need_two_bands); then
+// every word (16 k) of the row split into its one-band e4m3 rows
+// (split_word1), written in the compact layout the MMA reads (Item::bsrc,
+// words past K zero).  A chunk holds at most 28 stages (m = 2), so each
+// thread keeps its words in registers and all loads are in flight at once.
+// A chunk in which some row needs band B is built by the persistent kernel
+// from x and these maxima instead (rare: activations with outlier channels).
 constexpr int kPrepThreads = 128;
 constexpr int kPrepWords = 7;           // words per thread: 28 stages * 32 / 128
 constexpr uint32_t kBulkPiece = 16384;  // bytes per bulk copy of a prepared chunk
+// Per-chunk metadata (32 words): for activation row i, [2i] its maximum and
+// [2i + 1] its band-B maximum (fp32 bits of |x|), [16 + i] 1 if it needs
+// band B.
+constexpr int kMetaWords = 32;
 
 struct PrepItem {
     const uint16_t *x;
     unsigned char *b;
-    uint32_t *xmax;
+    uint32_t *meta;
     int k, m, stages, cstages;
     int task0;  // first task of the item; task task0 + c * m + i is chunk c, row i
 };
@@ -213,14 +232,51 @@ struct PrepParams {
     PrepItem item[kMaxItems];
 };
 
+// Maximum (or sum) of v over the CTA of k_tern_bprep; every thread gets it.
+__device__ __forceinline__ uint32_t prep_cta_max(uint32_t v, uint32_t *red)
+{
+    v = __reduce_max_sync(0xFFFFFFFFu, v);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < kPrepThreads / 32; ++w) v = max(v, red[w]);
+    __syncthreads();  // red is reused by the next reduction
+    return v;
+}
+
+__device__ __forceinline__ uint32_t prep_cta_add(uint32_t v, uint32_t *red)
+{
+    v = __reduce_add_sync(0xFFFFFFFFu, v);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    v = 0;
+#pragma unroll
+    for (int w = 0; w < kPrepThreads / 32; ++w) v += red[w];
+    __syncthreads();
+    return v;
+}
+
+__device__ __forceinline__ float prep_cta_addf(float v, float *red)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    v = 0.f;
+#pragma unroll
+    for (int w = 0; w < kPrepThreads / 32; ++w) v += red[w];
+    __syncthreads();
+    return v;
+}
+
 __global__ void __launch_bounds__(kPrepThreads) k_tern_bprep(const __grid_constant__ PrepParams p)
 {
-    __shared__ uint32_t wmax[kPrepThreads / 32];
+    __shared__ uint32_t red[kPrepThreads / 32];
     // The persistent kernel that follows may start at once: its weight stream
     // needs nothing from here, and its staging warps wait for this grid to
-    // finish before they read the workspace.  (A prep CTA fits on an SM
-    // beside a persistent CTA.)  The previous kernel on the stream may still
-    // read the workspace, and x may come from it: wait for it.
+    // finish before they read the workspace.  The previous kernel on the
+    // stream may still read the workspace, and x may come from it: wait for
+    // it.
     ptx::grid_dep_launch();
     ptx::grid_dep_wait();
     const int tid = (int)threadIdx.x, task = (int)blockIdx.x;
@@ -233,7 +289,6 @@ __global__ void __launch_bounds__(kPrepThreads) k_tern_bprep(const __grid_consta
     const int kw = it.k / 16;
     const uint4 *xr = reinterpret_cast<const uint4 *>(it.x + (size_t)mm * it.k);  // 2 x uint4 per word
     uint4 va[kPrepWords], vb[kPrepWords];
-    uint32_t mx = 0;
 #pragma unroll
     for (int q = 0; q < kPrepWords; ++q) {
         const int wi = tid + q * kPrepThreads, gw = w0 + wi;
@@ -243,26 +298,39 @@ __global__ void __launch_bounds__(kPrepThreads) k_tern_bprep(const __grid_consta
             vb[q] = __ldg(xr + 2 * gw + 1);
         }
     }
+    uint32_t mx = 0;
 #pragma unroll
     for (int q = 0; q < kPrepWords; ++q) mx = max(mx, max_abs16(va[q], vb[q]));
-    mx = __reduce_max_sync(0xFFFFFFFFu, mx);
-    if ((tid & 31) == 0) wmax[tid >> 5] = mx;
-    __syncthreads();
+    const uint32_t ma = prep_cta_max(mx, red);
+    const uint32_t tb2 = band_threshold2(ma);
+    uint32_t n = 0, mb = 0;
+    float sabs = 0.f;
 #pragma unroll
-    for (int w = 0; w < kPrepThreads / 32; ++w) mx = max(mx, wmax[w]);
-    if (tid == 0) it.xmax[8 * c + mm] = mx;
-    const float sc = exp2i(row_scale_exp(mx));
-    const size_t wbytes = 32u * (size_t)it.m;
+    for (int q = 0; q < kPrepWords; ++q) {
+        band_stats16(va[q], vb[q], tb2, n, sabs);
+        mb = max(mb, max_abs16_below(va[q], vb[q], tb2));
+    }
+    mb = prep_cta_max(mb, red);
+    n = prep_cta_add(n, red);
+    sabs = prep_cta_addf(sabs, reinterpret_cast<float *>(red));
+    if (tid == 0) {
+        uint32_t *meta = it.meta + (size_t)kMetaWords * c;
+        meta[2 * mm] = ma;
+        meta[2 * mm + 1] = mb;
+        meta[16 + mm] = need_two_bands(ma, n, sabs) ? 1u : 0u;
+    }
+    const float sc = exp2i(row_scale_exp(ma));
+    const size_t wbytes = b_block_bytes(it.m, 1);
     unsigned char *dst = it.b + (size_t)w0 * wbytes + 32u * (size_t)mm;
 #pragma unroll
     for (int q = 0; q < kPrepWords; ++q) {
         const int wi = tid + q * kPrepThreads;
         if (wi < nw) {
-            uint4 hi4, lo4;
-            split_word(va[q], vb[q], sc, hi4, lo4);
+            uint4 rows[2];
+            split_word1(va[q], vb[q], sc, rows);
             uint4 *d = reinterpret_cast<uint4 *>(dst + (size_t)wi * wbytes);
-            d[0] = hi4;
-            d[1] = lo4;
+            d[0] = rows[0];
+            d[1] = rows[1];
         }
     }
 }
@@ -278,6 +346,9 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
     const uint32_t bbuf = base + kOffB;
     float *xch = reinterpret_cast<float *>(gbase + kOffXch);
     const uint32_t bars = base + kOffBar;
+#ifdef TERN_WAIT_DIAG
+    if (threadIdx.x == 0 && blockIdx.x == 0) printf("k_tern_batched barriers at %u\n", bars);
+#endif
     uint32_t *words = reinterpret_cast<uint32_t *>(gbase + kOffBar + kWordsOff);
     volatile uint32_t *abort_flag = words + 1;
 
@@ -297,7 +368,9 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
         }
         ptx::mbar_init(bars + kBarDrain, kDecGroups * kCols);
         for (int j = 0; j < kCols * kDecGroups; ++j) ptx::mbar_init(bars + kBarTurn + 8 * j, 1);
-        for (int j = 1; j < 32; ++j) words[j] = 0u;
+        for (int j = 1; j < (int)kWordsCount; ++j) words[j] = 0u;
+        // no chunk's tag in the band words yet (a zero word would read as chunk 0's)
+        words[8 + 16] = words[8 + kXmWords + 16] = ~0u;
         ptx::fence_proxy_async_smem();
     }
     if (warp == 0) {
@@ -310,7 +383,7 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
     ptx::tc_fence_after();
     const uint32_t tmem = words[0];
     if (tid == 0) ptx::grid_dep_launch();
-    const Waiter waiter{abort_flag, &g_batched_error};
+    const Waiter waiter(abort_flag, &g_batched_error, p.wait_limit);
     Cursor cur;
     const bool any = cur.begin(&p, (int)blockIdx.x);
 
@@ -353,7 +426,7 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
         // TMEM slot g (quad q owns TMEM lanes 32q..32q+31), the group meets
         // at a named barrier, and then warp q issues the four K=32 steps of
         // column q (tcgen05.mma kind::f8f6f4, A from TMEM, B from shared
-        // memory, M = 128, N = 16) into D[buf][q].  Stage s's MMAs on a column
+        // memory, M = 128, N = 16 or 32) into D[buf][q].  Stage s's MMAs on a column
         // follow stage s-1's, issued by the previous group, through that
         // column's turn barriers (tcgen05 fence, mbarrier, fence), which order
         // the accumulation; a warp issues for one stage in three, so one
@@ -361,16 +434,16 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
         // warp issues an MMA about every 54 cycles, warps overlap).  Every
         // slot a group waits on was last used by the group itself, so no
         // phase-parity wait runs two phases ahead of its barrier.  A chunk's
-        // first-stage issuers wait for its B and D buffers (later stages see
-        // them through the turn chain); its last-stage issuers commit the
-        // chunk's D and B, which tracks the whole accumulation chain.
+        // first-stage issuers wait for its B buffer and for the epilogue
+        // that last read its accumulator columns (later stages see both
+        // through the turn chain); its last-stage issuers commit the chunk's
+        // D and B, which tracks the whole accumulation chain.
         const int g = (warp - kFirstDec) >> 2;
         const int quad = warp & 3;
         const int i = quad * 32 + lane;
         const uint32_t tm_row = tmem + ((uint32_t)(quad * 32) << 16);
         const uint32_t row_addr = wbuf + (uint32_t)i * 128u;
         const uint32_t sw = (uint32_t)(i & 7);  // 128-byte swizzle: 16-byte chunk c of row i sits at c ^ (i & 7)
-        const uint32_t a_col = tmem + (uint32_t)(g * 128 + quad * 32);  // column q of slot g (lane 0)
         const uint32_t my_turn = bars + kBarTurn + 8u * (uint32_t)(kDecGroups * quad + g);
         const uint32_t next_turn = bars + kBarTurn + 8u * (uint32_t)(kDecGroups * quad + (g + 1) % kDecGroups);
         const uint32_t a_empty = bars + kBarAEmpty + 8u * (uint32_t)g;
@@ -384,7 +457,47 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
         while (more) {
             const int n_st = cur.n_stages_chunk;
             const int buf = gc & 1;
-            const uint32_t wbytes = 32u * (uint32_t)p.item[cur.item].m;
+            const int m = p.item[cur.item].m;
+            // The epilogue that last read this buffer's accumulators (chunk
+            // gc - 2's) must be done; for gc < 2 that is the phase a fresh
+            // barrier counts as complete.
+            const uint32_t dempty = bars + kBarDEmpty + 8u * (uint32_t)buf;
+            const uint32_t dpar = ((uint32_t)(gc >> 1) & 1u) ^ 1u;
+            // The chunk's band count, written by the staging warps before its
+            // BFull arrival, is read after this issuer's first turn wait in
+            // the chunk (the turn chain starts at the stage-0 issuer, which
+            // waited for BFull); then its MMA shape and descriptors hold for
+            // the rest of the chunk.
+            const volatile uint32_t *bands_word = words + 8 + kXmWords * buf + 16;
+            const uint32_t tag = (uint32_t)gc & 0x3FFFFFFFu;
+            uint32_t bw = ~0u;  // this issuer's copy of the band word (no chunk's tag yet)
+            int cols = 0, steps = 0;
+            uint32_t idesc = 0, d = 0, a = 0, bd_lo0 = 0, bd_hi = 0, t_step = 0, st_step = 0, shape_of = ~0u;
+            // MMA shape and B descriptors of the chunk for band word bw:
+            // four 128-code columns at N = 16; two 256-code columns, issued
+            // by warps 0 and 1, at N = 32 (warps 2 and 3 then keep the turn
+            // and barrier protocol but issue nothing)
+            auto set_shape = [&](uint32_t bw) {
+                if (bw == shape_of) return;
+                shape_of = bw;
+                const int bands = (int)(bw & 3u) == 2 ? 2 : 1;
+                const int n = mma_n(m, bands);
+                const uint32_t wbytes = b_block_bytes(m, bands);
+                cols = n == 32 ? 2 : kCols;
+                steps = 16 / cols;  // K = 32 steps per column
+                idesc = idesc_n(n);
+                d = tmem + kDCol + (uint32_t)(n * (cols * buf + quad));
+                a = tmem + (uint32_t)(g * 128 + quad * 8 * steps);  // 8 columns per step
+                // compact B: column q of stage st starts at word st*32 + 2*steps*q, its
+                // K=32 step t at A column +8t and B word +2t; a two-band chunk fills
+                // both B buffers from the first
+                const uint32_t bsrc = bbuf + (bands == 2 ? 0u : (uint32_t)buf * kBBufBytes);
+                const uint64_t bd = b_desc_lbo(bsrc + (uint32_t)(2 * steps * quad) * wbytes, wbytes);
+                bd_lo0 = (uint32_t)bd;
+                bd_hi = (uint32_t)(bd >> 32);
+                t_step = (2u * wbytes) >> 4;
+                st_step = ((uint32_t)kStageWords * wbytes) >> 4;
+            };
             for (int st = (g - gs % kDecGroups + kDecGroups) % kDecGroups; st < n_st; st += kDecGroups) {
                 const uint32_t wf = bars + kBarWFull + 8 * w_r;
                 const uint32_t wpar = (uint32_t)w_q & 1u, apar = (uint32_t)a_q & 1u;
@@ -416,22 +529,43 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                 }
                 if (lane == 0) {
                     const uint32_t bpar = (uint32_t)(gc >> 1) & 1u;
-                    const uint32_t bfull = bars + kBarBFull + 8 * buf, dempty = bars + kBarDEmpty + 8 * buf;
-                    bool lok = st != 0 || ((ptx::mbar_try_wait(bfull, bpar) || waiter.wait(bfull, bpar)) &&
-                                           (ptx::mbar_try_wait(dempty, bpar ^ 1u) || waiter.wait(dempty, bpar ^ 1u)));
-                    lok = lok && (ptx::mbar_try_wait(my_turn, tpar) || waiter.wait(my_turn, tpar));
+                    const uint32_t bfull = bars + kBarBFull + 8 * buf;
+                    // The band word as it stands now, usually already this
+                    // chunk's (the staging warps run ahead): its MMA shape and
+                    // descriptors are then ready before the turn comes.
+                    if ((bw >> 2) != tag) {
+                        bw = *bands_word;
+                        set_shape(bw);
+                    }
+                    // The turn first: once it has come, chunk gc - 2 (the same B
+                    // buffer) has passed its own BFull wait and the epilogue
+                    // before the one waited for here is done, so neither
+                    // parity wait below can run ahead of its barrier (a wait
+                    // one phase early returns at once, taking the earlier
+                    // phase for this one).
+                    bool lok = ptx::mbar_try_wait(my_turn, tpar) || waiter.wait(my_turn, tpar);
+                    lok = lok && (st != 0 || ((ptx::mbar_try_wait(bfull, bpar) || waiter.wait(bfull, bpar)) &&
+                                              (ptx::mbar_try_wait(dempty, dpar) || waiter.wait(dempty, dpar))));
                     if (lok) {
                         ptx::tc_fence_after();
-                        const uint32_t d = tmem + kDCol + 16u * (uint32_t)(kCols * buf + quad);
-                        // compact B: 16-code blocks 32m bytes apart; column q of stage st at word st*32 + 8q
-                        const uint64_t bd = b_desc_lbo(bbuf + (uint32_t)buf * kBBufStride +
-                                                           (uint32_t)(st * kStageWords + 8 * quad) * wbytes,
-                                                       wbytes);
-                        const uint32_t bd_lo = (uint32_t)bd, bd_hi = (uint32_t)(bd >> 32), t_step = (2u * wbytes) >> 4;
-                        ptx::mma_ts_f8f6f4_lh(d, a_col, bd_lo, bd_hi, kIdesc, st != 0 ? 1u : 0u);
+                        // a word read before the waits may have been the previous
+                        // chunk's on this buffer: its tag tells, read it again
+                        if ((bw >> 2) != tag) {
+                            bw = *bands_word;
+                            set_shape(bw);
+                        }
+                        if (quad < cols) {
+                            const uint32_t bd_lo = bd_lo0 + st_step * (uint32_t)st;
+                            ptx::mma_ts_f8f6f4_lh(d, a, bd_lo, bd_hi, idesc, st != 0 ? 1u : 0u);
 #pragma unroll
-                        for (int t = 1; t < 4; ++t)  // K=32 step 4q+t: A columns +8t, B words +2t
-                            ptx::mma_ts_f8f6f4_lh(d, a_col + 8u * t, bd_lo + t_step * t, bd_hi, kIdesc, 1u);
+                            for (int t = 1; t < 4; ++t)
+                                ptx::mma_ts_f8f6f4_lh(d, a + 8u * t, bd_lo + t_step * t, bd_hi, idesc, 1u);
+                            if (cols == 2) {
+#pragma unroll
+                                for (int t = 4; t < 8; ++t)
+                                    ptx::mma_ts_f8f6f4_lh(d, a + 8u * t, bd_lo + t_step * t, bd_hi, idesc, 1u);
+                            }
+                        }
                         ptx::tc_fence_before();
                         ptx::mbar_arrive(next_turn);  // the next stage's MMAs on this column follow these
                         ptx::mma_commit(a_empty);
@@ -462,64 +596,108 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
         const int quad = warp & 3;
         const int i = quad * 32 + lane;               // tile row == TMEM lane
         ptx::grid_dep_wait();
-        float acc[8];
+        // per activation row, the unit's sum so far as an unevaluated pair
+        // (see acc_pair): chunks and bands of one unit have their own scales
+        float acc[8], acc_lo[8];
 #pragma unroll
-        for (int n = 0; n < 8; ++n) acc[n] = 0.f;
+        for (int n = 0; n < 8; ++n) acc[n] = acc_lo[n] = 0.f;
         // previous chunk, whose accumulators are read after the next chunk's B is staged
-        int prev_item = -1, prev_tile = 0;
+        int prev_item = -1, prev_tile = 0, prev_bands = 1;
         bool prev_last = false;
         int gc = 0;
         bool ok = any;
-        // what each B buffer holds: a chunk of an item is staged once and reused
-        // by every later tile of the same item that lands on this buffer
+        // what each B buffer holds: a one-band chunk of an item is staged once
+        // and reused by every later tile of the same item that lands on it
         int held_item[2] = {-1, -1}, held_chunk[2] = {-1, -1};
         int last_gc[2] = {-1, -1};  // last chunk whose BFull phase each buffer took part in
+        uint32_t *meta_s = words + 8;  // [kXmWords] per buffer: row maxima, then the band count at [16]
 
-        auto epilogue = [&](int e) {  // read chunk e's accumulators, finish the unit if it was its last chunk
+        // Reads chunk e's accumulators into the rows' pairs and finishes the
+        // unit if it was its last chunk.  Within a band the issuing columns
+        // and the hi/lo terms are summed in fp32 (one band, one scale); each
+        // band's total then goes into the row's pair.
+        auto epilogue = [&](int e) {
             const int eb = e & 1;
+            const Item &it = p.item[prev_item];
+            const uint32_t *xm = meta_s + kXmWords * eb;
+            const int bands = (int)(xm[16] & 3u);
+            const int n = mma_n(it.m, bands), cols = n == 32 ? 2 : kCols;
             uint32_t good = 1u;
             if (lane == 0) good = waiter.wait(bars + kBarDFull + 8 * eb, (e >> 1) & 1) ? 1u : 0u;
             good = __shfl_sync(0xFFFFFFFFu, good, 0);
-            float dsum[16];
-#pragma unroll
-            for (int n = 0; n < 16; ++n) dsum[n] = 0.f;
             if (good) {
                 ptx::tc_fence_after();
+                const uint32_t base = tmem + ((uint32_t)(quad * 32) << 16) + kDCol + (uint32_t)(n * cols * eb);
+                if (it.m == 1 && bands == 1) {  // the decode-time GEMV: two live columns
+                    float d0 = 0.f, d1 = 0.f;
 #pragma unroll 1
-                for (int a = 0; a < kCols; ++a) {
-                    uint32_t dv[16];
-                    ptx::tmem_ld_32x32b_x16(tmem + ((uint32_t)(quad * 32) << 16) + kDCol + 16u * (kCols * eb + a), dv);
-                    ptx::tmem_wait_ld();
+                    for (int c = 0; c < cols; ++c) {
+                        uint32_t dv[4];
+                        ptx::tmem_ld_32x32b_x4(base + (uint32_t)(n * c), dv);
+                        ptx::tmem_wait_ld();
+                        d0 += __uint_as_float(dv[0]);
+                        d1 += __uint_as_float(dv[1]);
+                    }
+                    const int sa = row_scale_exp(xm[0]);
+                    acc_pair(acc[0], acc_lo[0], fmaf(d1, exp2i(-sa - 4), d0 * exp2i(-sa)));
+                } else
 #pragma unroll
-                    for (int n = 0; n < 16; ++n) dsum[n] += __uint_as_float(dv[n]);
+                for (int h = 0; h < 2; ++h) {  // TMEM columns 16h .. 16h+15 of every issuing column
+                    if (16 * h >= 2 * bands * it.m) break;
+                    float dsum[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) dsum[q] = 0.f;
+#pragma unroll 1
+                    for (int c = 0; c < cols; ++c) {
+                        uint32_t dv[16];
+                        ptx::tmem_ld_32x32b_x16(base + (uint32_t)(n * c + 16 * h), dv);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) dsum[q] += __uint_as_float(dv[q]);
+                    }
+                    if (bands == 1) {  // column 2i: hi, 2i + 1: lo of row i (h == 0)
+#pragma unroll
+                        for (int mm = 0; mm < 8; ++mm) {
+                            if (h == 0 && mm < it.m) {
+                                const int sa = row_scale_exp(xm[2 * mm]);
+                                acc_pair(acc[mm], acc_lo[mm],
+                                         fmaf(dsum[2 * mm + 1], exp2i(-sa - 4), dsum[2 * mm] * exp2i(-sa)));
+                            }
+                        }
+                    } else {  // column 4i + b: hi_A, lo_A, hi_B, lo_B of row i
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const int mm = 4 * h + r;
+                            if (mm < it.m) {
+                                const int sa = row_scale_exp(xm[2 * mm]), sb = row_scale_exp(xm[2 * mm + 1]);
+                                acc_pair(acc[mm], acc_lo[mm],
+                                         fmaf(dsum[4 * r + 1], exp2i(-sa - 4), dsum[4 * r] * exp2i(-sa)));
+                                acc_pair(acc[mm], acc_lo[mm],
+                                         fmaf(dsum[4 * r + 3], exp2i(-sb - 4), dsum[4 * r + 2] * exp2i(-sb)));
+                            }
+                        }
+                    }
                 }
             }
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bars + kBarDEmpty + 8 * eb);
-            const Item &it = p.item[prev_item];
-            const uint32_t *xm = words + 8 + 8 * eb;
-#pragma unroll
-            for (int mm = 0; mm < 8; ++mm) {
-                if (mm < it.m) {
-                    const int s = row_scale_exp(xm[mm]);
-                    acc[mm] += dsum[2 * mm] * exp2i(-s) + dsum[2 * mm + 1] * exp2i(max(-s - 4, -126));
-                }
-            }
             if (!prev_last) return;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], acc_lo[q]);
             if (it.swiglu) {
                 const int r = prev_tile * 64 + (i & 63);
                 if (i >= 64 && r < it.rows) {
                     const float su = it.scale_u[r];
 #pragma unroll
-                    for (int n = 0; n < 8; ++n) xch[(i - 64) * 8 + n] = su * (0.5f * acc[n]);
+                    for (int q = 0; q < 8; ++q) xch[(i - 64) * 8 + q] = su * (0.5f * acc[q]);
                 }
                 ptx::named_bar_sync(1, kStagers);
                 if (i < 64 && r < it.rows) {
                     const float sg = it.scale_g[r];
 #pragma unroll
-                    for (int n = 0; n < 8; ++n)
-                        if (n < it.m) it.y[(size_t)n * it.rows + r] = silu_f(sg * (0.5f * acc[n])) * xch[i * 8 + n];
+                    for (int q = 0; q < 8; ++q)
+                        if (q < it.m) it.y[(size_t)q * it.rows + r] = silu_f(sg * (0.5f * acc[q])) * xch[i * 8 + q];
                 }
                 ptx::named_bar_sync(1, kStagers);  // xch reusable
             } else {
@@ -527,12 +705,44 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                 if (r < it.rows) {
                     const float sc = it.scale_g[r];
 #pragma unroll
-                    for (int n = 0; n < 8; ++n)
-                        if (n < it.m) it.y[(size_t)n * it.rows + r] = sc * (0.5f * acc[n]);
+                    for (int q = 0; q < 8; ++q)
+                        if (q < it.m) it.y[(size_t)q * it.rows + r] = sc * (0.5f * acc[q]);
                 }
             }
 #pragma unroll
-            for (int n = 0; n < 8; ++n) acc[n] = 0.f;
+            for (int q = 0; q < 8; ++q) acc[q] = acc_lo[q] = 0.f;
+        };
+
+        // Waits (lane 0 of each staging warp, then the warp) until chunk
+        // gc - 1's MMAs are done with the other B buffer: a two-band chunk
+        // takes both buffers, and so did a previous two-band chunk.
+        auto wait_other_buffer = [&]() {
+            if (gc >= 1 && lane == 0)
+                waiter.wait(bars + kBarBEmpty + 8 * ((gc - 1) & 1), (uint32_t)((gc - 1) >> 1) & 1u);
+            __syncwarp();
+        };
+        // Two-band operand of a chunk from x in global memory, with each
+        // row's maxima already in xm (both buffers, from the first; the
+        // callers have waited for them).
+        auto build_two_band = [&](const Item &it, int w0, int n_words, const uint32_t *xm) {
+            const int m = it.m, kw = it.k / 16;
+            const uint32_t wbytes = b_block_bytes(m, 2);
+#pragma unroll 1
+            for (int item = st_tid; item < m * n_words; item += kStagers) {
+                const int mm = item / n_words, wi = item - mm * n_words, gw = w0 + wi;
+                uint4 va = make_uint4(0u, 0u, 0u, 0u), vb = va;
+                if (gw < kw) {
+                    const uint4 *xr = reinterpret_cast<const uint4 *>(it.x + (size_t)mm * it.k) + 2 * gw;
+                    va = xr[0];
+                    vb = xr[1];
+                }
+                uint4 rows[4];
+                split_word2(va, vb, exp2i(row_scale_exp(xm[2 * mm])), exp2i(row_scale_exp(xm[2 * mm + 1])),
+                            band_threshold2(xm[2 * mm]), rows);
+                const uint32_t at = bbuf + (uint32_t)wi * wbytes + 64u * (uint32_t)mm;
+#pragma unroll
+                for (int r = 0; r < 4; ++r) ptx::sts128(at + 16u * (uint32_t)r, rows[r]);
+            }
         };
 
         while (ok) {
@@ -540,98 +750,125 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
             const Item &it = p.item[cur.item];
             // the MMAs of chunk gc-2 must be done with this B buffer
             if (lane == 0) waiter.wait(bars + kBarBEmpty + 8 * buf, ((gc >> 1) & 1) ^ 1);
-            uint32_t *xm = words + 8 + 8 * buf;
+            __syncwarp();
+            if (prev_bands == 2) wait_other_buffer();
+            uint32_t *xm = meta_s + kXmWords * buf;
             const bool reuse = held_item[buf] == cur.item && held_chunk[buf] == cur.chunk;
             // Past this barrier every staging warp has finished chunk gc-2's
-            // epilogue, the last reader of this buffer's row maxima xm.  The
+            // epilogue, the last reader of this buffer's metadata xm.  The
             // barrier ORs the abort flag over the four staging warps, so they
             // all take the same branch.
             if (ptx::named_bar_or(1, kStagers, *abort_flag != 0u)) break;
-            if (reuse) {  // B (and its row scales) already hold this chunk
-                last_gc[buf] = gc;
-                ptx::mbar_arrive(bars + kBarBFull + 8 * buf);
-                if (gc >= 1) epilogue(gc - 1);
-                prev_item = cur.item;
-                prev_tile = cur.tile;
-                prev_last = cur.last_chunk_of_unit();
-                ++gc;
-                ok = cur.next_chunk();
-                continue;
-            }
-            const int n_words = cur.n_stages_chunk * kStageWords;
-            const int k0 = cur.chunk * cur.cstages * kStageWords * 16;
-            const int m = it.m;
-            const int n_items = m * n_words;
-            const uint32_t bb = bbuf + (uint32_t)buf * kBBufStride;
-            const uint32_t wbytes = 32u * (uint32_t)m;  // compact B: a block holds rows 0..2m-1
+            int bands = 1;
             const uint32_t bfull = bars + kBarBFull + 8 * buf;
-            if (it.bsrc != nullptr) {
-                // prepared: the chunk's bytes in a few bulk copies that
-                // complete on BFull (its phase also waits for every staging
-                // thread's arrival below), and the chunk's row maxima
-                if (st_tid == 0) {
-                    const uint32_t bytes = (uint32_t)n_words * wbytes;
-                    const unsigned char *src = it.bsrc + (size_t)(k0 / 16) * wbytes;
-                    ptx::mbar_expect_tx(bfull, bytes);
-                    for (uint32_t o = 0; o < bytes; o += kBulkPiece)
-                        ptx::bulk_load(bb + o, src + o, min(kBulkPiece, bytes - o), bfull);
+            if (!reuse) {
+                const int m = it.m;
+                const int n_words = cur.n_stages_chunk * kStageWords;
+                const int w0 = cur.chunk * cur.cstages * kStageWords;
+                if (it.bsrc != nullptr) {
+                    // prepared: the rows' maxima and band-B flags; with one
+                    // band the chunk's bytes in a few bulk copies that complete
+                    // on BFull (whose phase also waits for every staging
+                    // thread's arrival below), with two a build from x here
+                    const uint32_t *meta = it.meta + (size_t)kMetaWords * cur.chunk;
+                    uint32_t two = 0;
+                    for (int q = 0; q < m; ++q) two |= meta[16 + q];
+                    bands = two != 0u ? 2 : 1;
+                    if (st_tid < 2 * m) xm[st_tid] = meta[st_tid];
+                    if (bands == 1) {
+                        if (st_tid == 0) {
+                            const uint32_t bytes = (uint32_t)n_words * b_block_bytes(m, 1);
+                            const unsigned char *src = it.bsrc + (size_t)w0 * b_block_bytes(m, 1);
+                            const uint32_t bb = bbuf + (uint32_t)buf * kBBufBytes;
+                            ptx::mbar_expect_tx(bfull, bytes);
+                            for (uint32_t o = 0; o < bytes; o += kBulkPiece)
+                                ptx::bulk_load(bb + o, src + o, min(kBulkPiece, bytes - o), bfull);
+                        }
+                    } else {
+                        if (prev_bands != 2) wait_other_buffer();
+                        ptx::named_bar_sync(1, kStagers);  // xm complete
+                        build_two_band(it, w0, n_words, xm);
+                        ptx::fence_proxy_async_smem();  // my B writes -> visible to the tensor core
+                    }
+                } else {
+                    // Built here (m = 1 items).  The row's words are copied
+                    // asynchronously into their one-band slots (32 bytes each,
+                    // the size of 16 bf16; zero-filled past K); the row
+                    // maximum is reduced from shared memory; then each word's
+                    // band statistics are taken and the word is split in place
+                    // with one band.  If the row needs band B (need_two_bands)
+                    // the chunk is built again with two bands from x in
+                    // global memory, in both buffers.  A warp's 32 items are
+                    // 32 consecutive words of the row.
+                    const uint32_t bb = bbuf + (uint32_t)buf * kBBufBytes;
+                    float *sabs = reinterpret_cast<float *>(xm + 18);
+                    if (st_tid == 0) {
+                        xm[0] = xm[1] = xm[17] = 0u;
+                        *sabs = 0.f;
+                    }
+                    for (int wi = st_tid; wi < n_words; wi += kStagers) {
+                        const int kk = 16 * (w0 + wi);
+                        const bool in_k = kk < it.k;
+                        const uint16_t *src = in_k ? it.x + kk : it.x;
+                        ptx::cp_async16(bb + 32u * (uint32_t)wi, src, in_k ? 16u : 0u);
+                        ptx::cp_async16(bb + 32u * (uint32_t)wi + 16u, src + 8, in_k ? 16u : 0u);
+                    }
+                    ptx::cp_async_wait_all();
+                    ptx::named_bar_sync(1, kStagers);
+                    for (int wi = st_tid; wi < n_words; wi += kStagers) {
+                        const uint32_t at = bb + 32u * (uint32_t)wi;
+                        const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, max_abs16(ptx::lds128(at), ptx::lds128(at + 16u)));
+                        if (lane == 0) atomicMax(&xm[0], mx);
+                    }
+                    ptx::named_bar_sync(1, kStagers);
+                    const uint32_t tb2 = band_threshold2(xm[0]);
+                    const float sca = exp2i(row_scale_exp(xm[0]));
+                    for (int wi = st_tid; wi < n_words; wi += kStagers) {
+                        const uint32_t at = bb + 32u * (uint32_t)wi;
+                        const uint4 va = ptx::lds128(at), vb = ptx::lds128(at + 16u);
+                        uint32_t cnt = 0;
+                        float sa = 0.f;
+                        band_stats16(va, vb, tb2, cnt, sa);
+                        const uint32_t mb = __reduce_max_sync(0xFFFFFFFFu, max_abs16_below(va, vb, tb2));
+                        cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) sa += __shfl_xor_sync(0xFFFFFFFFu, sa, o);
+                        if (lane == 0) {
+                            atomicMax(&xm[1], mb);
+                            atomicAdd(&xm[17], cnt);
+                            atomicAdd(sabs, sa);
+                        }
+                        uint4 rows[2];
+                        split_word1(va, vb, sca, rows);
+                        ptx::sts128(at, rows[0]);
+                        ptx::sts128(at + 16u, rows[1]);
+                    }
+                    ptx::named_bar_sync(1, kStagers);
+                    bands = need_two_bands(xm[0], xm[17], *sabs) ? 2 : 1;
+                    if (bands == 2) {
+                        if (prev_bands != 2) wait_other_buffer();
+                        ptx::named_bar_sync(1, kStagers);  // both buffers are free
+                        build_two_band(it, w0, n_words, xm);
+                    }
+                    ptx::fence_proxy_async_smem();  // my B writes -> visible to the tensor core
                 }
-                if (st_tid < m) xm[st_tid] = it.xmax[8 * cur.chunk + st_tid];
-                held_item[buf] = cur.item;
-                held_chunk[buf] = cur.chunk;
-                last_gc[buf] = gc;
-                ptx::mbar_arrive(bfull);
-                if (gc >= 1) epilogue(gc - 1);
-                prev_item = cur.item;
-                prev_tile = cur.tile;
-                prev_last = cur.last_chunk_of_unit();
-                ++gc;
-                ok = cur.next_chunk();
-                continue;
+                if (st_tid == 0) xm[16] = ((uint32_t)gc << 2) | (uint32_t)bands;
+                if (bands == 2) {  // both buffers are overwritten: neither holds a reusable chunk
+                    held_item[0] = held_item[1] = -1;
+                } else {
+                    held_item[buf] = cur.item;
+                    held_chunk[buf] = cur.chunk;
+                }
+            } else if (st_tid == 0) {
+                xm[16] = ((uint32_t)gc << 2) | 1u;  // the same one-band chunk again, under this chunk's number
             }
-            if (st_tid < 8) xm[st_tid] = 0u;
-            ptx::named_bar_sync(1, kStagers);
-            // The compact layout keeps 32 bytes (hi and lo rows) per 16
-            // activations of a row, the size of the 16 bf16 values, so each
-            // word is copied asynchronously to its final place (all copies in
-            // flight at once, zero-filled past K), its row maximum reduced
-            // from shared memory, and split in place.  A warp's 32 items are
-            // 32 consecutive words of one activation row (n_words is a
-            // multiple of 32), so the maximum is reduced in the warp first.
-            for (int item = st_tid; item < n_items; item += kStagers) {
-                const int mm = item / n_words, wi = item - mm * n_words;
-                const int kk = k0 + 16 * wi;
-                const bool in_k = kk < it.k;
-                const uint16_t *src = in_k ? it.x + (size_t)mm * it.k + kk : it.x;
-                const uint32_t at = bb + (uint32_t)wi * wbytes + 32u * (uint32_t)mm;
-                ptx::cp_async16(at, src, in_k ? 16u : 0u);
-                ptx::cp_async16(at + 16u, src + 8, in_k ? 16u : 0u);
-            }
-            ptx::cp_async_wait_all();
-            for (int item = st_tid; item < n_items; item += kStagers) {
-                const int mm = item / n_words, wi = item - mm * n_words;
-                const uint32_t at = bb + (uint32_t)wi * wbytes + 32u * (uint32_t)mm;
-                const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, max_abs16(ptx::lds128(at), ptx::lds128(at + 16u)));
-                if (lane == 0) atomicMax(&xm[mm], mx);
-            }
-            ptx::named_bar_sync(1, kStagers);
-            for (int item = st_tid; item < n_items; item += kStagers) {
-                const int mm = item / n_words, wi = item - mm * n_words;
-                const uint32_t at = bb + (uint32_t)wi * wbytes + 32u * (uint32_t)mm;
-                uint4 hi4, lo4;
-                split_word(ptx::lds128(at), ptx::lds128(at + 16u), exp2i(row_scale_exp(xm[mm])), hi4, lo4);
-                ptx::sts128(at, hi4);
-                ptx::sts128(at + 16u, lo4);
-            }
-            held_item[buf] = cur.item;
-            held_chunk[buf] = cur.chunk;
             last_gc[buf] = gc;
-            ptx::fence_proxy_async_smem();  // my B writes -> visible to the tensor core
             ptx::mbar_arrive(bfull);
             if (gc >= 1) epilogue(gc - 1);
             prev_item = cur.item;
             prev_tile = cur.tile;
             prev_last = cur.last_chunk_of_unit();
+            prev_bands = bands;
             ++gc;
             ok = cur.next_chunk();
         }
@@ -692,10 +929,10 @@ std::vector<int> plan_groups(const tern_batch_item *items, int n)
     return even.size() <= greedy.size() ? even : greedy;
 }
 
-// Workspace of prepared activations per (device, stream), grown on demand.
+// Workspace of prepared activations per (context, stream), grown on demand.
 // A grown-out buffer is never freed: a launch captured in a CUDA graph keeps
 // the address it was captured with.  Returns nullptr if the allocation fails
-// (the staging warps then build B themselves).
+// (the call then returns TERN_ERR_CUDA; the groups before it have launched).
 void *workspace(cudaStream_t stream, size_t need)
 {
     struct Buf {
@@ -703,11 +940,13 @@ void *workspace(cudaStream_t stream, size_t need)
         size_t bytes = 0;
     };
     static std::mutex mu;
-    static std::map<std::pair<int, cudaStream_t>, Buf> all;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    static std::map<std::pair<unsigned long long, cudaStream_t>, Buf> all;
+    // keyed by the current context: a context created after a device reset
+    // gets buffers of its own
+    const unsigned long long ctx = current_context_id();
+    if (ctx == 0) return nullptr;
     std::lock_guard<std::mutex> lock(mu);
-    Buf &b = all[{dev, stream}];
+    Buf &b = all[{ctx, stream}];
     if (b.bytes >= need) return b.p;
     const size_t bytes = need > 2 * b.bytes ? need : 2 * b.bytes;
     // an allocation is allowed while a stream of this thread is being captured
@@ -733,16 +972,17 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 void chunk_plan(int k, int m, int &stages, int &cstages)
 {
     stages = (k / 16 + kStageWords - 1) / kStageWords;
-    const int cap = kBBufBytes / (1024 * m);  // stages of compact B one buffer holds
+    const int cap = kBBufBytes / (kStageWords * (int)b_block_bytes(m, 1));  // stages of one-band B one buffer holds
     const int n_chunks = (stages + cap - 1) / cap;
     cstages = (stages + n_chunks - 1) / n_chunks;
 }
 
-// Workspace bytes of one prepared item (see Item::bsrc, Item::xmax).
+// Workspace bytes of one prepared item (see Item::bsrc, Item::meta).
+size_t prep_b_bytes(int stages, int m) { return align256((size_t)stages * kStageWords * b_block_bytes(m, 1)); }
 size_t prep_bytes(int stages, int cstages, int m)
 {
     const int n_chunks = (stages + cstages - 1) / cstages;
-    return align256((size_t)stages * 1024u * (size_t)m) + align256((size_t)n_chunks * 8u * sizeof(uint32_t));
+    return prep_b_bytes(stages, m) + align256((size_t)n_chunks * kMetaWords * sizeof(uint32_t));
 }
 
 // Scratch of tern_gemm_batched_noalloc: module-scope device memory, which the
@@ -780,15 +1020,19 @@ tern_status run_batched(const tern_batch_item *items, int n, cudaStream_t stream
 {
     static_assert(sizeof(Params) + sizeof(Maps) < 32000, "kernel parameters exceed 32 KB");
     const int sms = sm_count();
-    // the kernel's shared-memory attribute, once per device
-    static bool attr_set[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TERN_ERR_CUDA;
-    if (!attr_set[dev]) {
-        if (cudaFuncSetAttribute(k_tern_batched, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-            cudaSuccess)
-            return TERN_ERR_CUDA;
-        attr_set[dev] = true;
+    // the kernel's shared-memory attribute, once per context (a context
+    // created after a device reset starts without it)
+    {
+        static std::mutex mu;
+        static std::set<unsigned long long> done;
+        const unsigned long long ctx = current_context_id();
+        std::lock_guard<std::mutex> lock(mu);
+        if (ctx == 0 || done.count(ctx) == 0) {
+            if (cudaFuncSetAttribute(k_tern_batched, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
+                cudaSuccess)
+                return TERN_ERR_CUDA;
+            if (ctx != 0) done.insert(ctx);
+        }
     }
     int begin = 0;
     for (const int end : plan_groups(items, n)) {
@@ -802,7 +1046,7 @@ tern_status run_batched(const tern_batch_item *items, int n, cudaStream_t stream
             const tern_batch_item &b = items[idx];
             if (b.w->rows == 0) continue;
             if (b.w->k == 0) {  // empty sum: y = scale * 0
-                const tern_status st = gemm_cc(b.w, b.up, b.x, b.m, b.y, stream);
+                const tern_status st = empty_sum(b.w, b.up, b.m, b.y, stream);
                 if (st != TERN_OK) return st;
                 continue;
             }
@@ -830,10 +1074,13 @@ tern_status run_batched(const tern_batch_item *items, int n, cudaStream_t stream
         begin = end;
         if (cnt == 0) continue;
         prm.n_items = cnt;
+        prm.wait_limit = wait_limit();
 
         // Items with m >= 2 take their B from the workspace, written by one
-        // k_tern_bprep launch just before: per item the padded K's words
-        // (1024m bytes per stage), then 8 row maxima per chunk.
+        // k_tern_bprep launch just before (one CTA per item, K chunk and
+        // activation row): per item the padded K's one-band words (1024m
+        // bytes per stage), then kMetaWords of metadata per chunk.  Items
+        // with m = 1 are built by the persistent kernel's staging warps.
         PrepParams pp;
         std::memset(&pp, 0, sizeof(pp));
         size_t ws_need = 0;
@@ -841,29 +1088,28 @@ tern_status run_batched(const tern_batch_item *items, int n, cudaStream_t stream
         for (int j = 0; j < cnt; ++j) {
             const Item &it = prm.item[j];
             if (it.m < 2) continue;
-            const int n_chunks = (it.stages + it.cstages - 1) / it.cstages;
-            if (it.cstages * kStageWords > kPrepWords * kPrepThreads) return TERN_ERR_SHAPE;  // cannot happen: m >= 2
             ws_off[j].first = ws_need;
-            ws_off[j].second = ws_need + align256((size_t)it.stages * 1024u * (size_t)it.m);
+            ws_off[j].second = ws_need + prep_b_bytes(it.stages, it.m);
             ws_need += prep_bytes(it.stages, it.cstages, it.m);
         }
-        unsigned char *ws = nullptr;
-        if (ws_need > 0) ws = fixed_ws != nullptr ? fixed_ws : static_cast<unsigned char *>(workspace(stream, ws_need));
-        if (ws != nullptr) {
+        if (ws_need > 0) {
+            unsigned char *ws = fixed_ws != nullptr ? fixed_ws : static_cast<unsigned char *>(workspace(stream, ws_need));
+            if (ws == nullptr) return TERN_ERR_CUDA;
             for (int j = 0; j < cnt; ++j) {
                 Item &it = prm.item[j];
                 if (it.m < 2) continue;
                 it.bsrc = ws + ws_off[j].first;
-                it.xmax = reinterpret_cast<const uint32_t *>(ws + ws_off[j].second);
+                it.meta = reinterpret_cast<const uint32_t *>(ws + ws_off[j].second);
                 PrepItem &q = pp.item[pp.n_items++];
                 q.x = it.x;
                 q.b = ws + ws_off[j].first;
-                q.xmax = reinterpret_cast<uint32_t *>(ws + ws_off[j].second);
+                q.meta = reinterpret_cast<uint32_t *>(ws + ws_off[j].second);
                 q.k = it.k;
                 q.m = it.m;
                 q.stages = it.stages;
                 q.cstages = it.cstages;
                 q.task0 = pp.n_tasks;
+                if (it.cstages * kStageWords > kPrepWords * kPrepThreads) return TERN_ERR_SHAPE;  // cannot happen: m >= 2
                 pp.n_tasks += (it.stages + it.cstages - 1) / it.cstages * it.m;
             }
             cudaLaunchConfig_t pcfg = {};
@@ -940,19 +1186,26 @@ tern_status gemm_batched_noalloc(const tern_batch_item *items, int n, cudaStream
         if (need > (size_t)TERN_NOALLOC_WS_BYTES) return TERN_ERR_SHAPE;
         begin = end;
     }
-    // the scratch's device address, looked up once per device
+    // The scratch's device address, looked up with the device current the
+    // first time a context uses this entry point.  The cache is keyed by the
+    // context, so a context created after a device reset (whose module, and
+    // array, are new) looks the address up again.
     static std::mutex mu;
-    static void *addr[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return TERN_ERR_CUDA;
+    static std::map<unsigned long long, void *> addr;
+    const unsigned long long ctx = current_context_id();
     void *ws = nullptr;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (addr[dev] == nullptr && cudaGetSymbolAddress(&addr[dev], g_noalloc_ws) != cudaSuccess) {
-            addr[dev] = nullptr;
-            return TERN_ERR_CUDA;
+        auto f = ctx != 0 ? addr.find(ctx) : addr.end();
+        if (f != addr.end()) {
+            ws = f->second;
+        } else {
+            if (cudaGetSymbolAddress(&ws, g_noalloc_ws) != cudaSuccess || ws == nullptr) {
+                (void)cudaGetLastError();
+                return TERN_ERR_CUDA;
+            }
+            if (ctx != 0) addr[ctx] = ws;
         }
-        ws = addr[dev];
     }
     return run_batched(items, n, stream, static_cast<unsigned char *>(ws));
 }

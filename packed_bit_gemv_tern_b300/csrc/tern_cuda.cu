@@ -1,93 +1,25 @@
-// tern_cuda.cu -- device entry points of the C ABI and their CUDA kernels.
+// tern_cuda.cu -- host side of the C ABI's device entry points: argument
+// checks, the choice of kernel, the debug unpack kernel and the empty-sum
+// kernel.
 //
 // What is computed (Neutrino-1 8B model page, intro and "Where the bytes
 // live"): y[m][r] = scale[r] * sum_k t[r][k] * x[m][k] with t in {-1,0,+1}
 // stored 2 bits per weight and decoded inside the kernel; the gated pair
 // h = silu(gate x) * (up x) follows the spec table's SwiGLU feed-forward.
-//
-// This file holds the CUDA-core kernels: the packed-weight stream is read
-// with 128-bit read-only loads, every 2-bit code is decoded with bit
-// operations into a sign-selected add of the activation (no multiply by a
-// weight), partial sums stay in fp32 registers and warps reduce with shuffles.
+// Every product with K > 0 runs on the tensor-core kernels (tern_mma.cu for
+// one product per call, tern_batched.cu for batches); K == 0 has no weights
+// to stream and is written by k_empty_sum.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 
 #include "tern.h"
 #include "tern_internal.cuh"
+#include "tern_mma_common.cuh"
 
 namespace tern {
-
-// ---------------------------------------------------------------------------
-// Device helpers
-// ---------------------------------------------------------------------------
-
-// Streaming 128-bit load of packed weights: read-only path, no L1 allocation
-// (each weight byte is used once per call).
-__device__ __forceinline__ uint4 ld_stream_u4(const void *p)
-{
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
-
-__device__ __forceinline__ float bf16lo(uint32_t pair) { return __uint_as_float(pair << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t pair) { return __uint_as_float(pair & 0xFFFF0000u); }
-
-// Sign-select for one 2-bit field c = (b1,b0): b0 keeps x, b1 flips its sign.
-// Valid fields: 00 -> +0/-0 contribution of magnitude 0, 01 -> x, 11 -> -x.
-// The invalid field 10 contributes 0.  Done entirely with integer bit ops on
-// the fp32 pattern of x: mask = -(b0) keeps or clears every bit, and b1 is
-// moved onto the sign bit.
-__device__ __forceinline__ float sign_select(uint32_t field, float x)
-{
-    const uint32_t b0 = field & 1u;
-    const uint32_t keep = 0u - b0;                 // all ones when b0 = 1
-    const uint32_t flip = (field & 2u) << 30;      // b1 onto bit 31
-    return __uint_as_float((__float_as_uint(x) & keep) ^ (flip & keep));
-}
-
-__device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
-
-template <int M>
-__device__ __forceinline__ void warp_reduce(float (&a)[M])
-{
-#pragma unroll
-    for (int m = 0; m < M; ++m) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) a[m] += __shfl_xor_sync(0xFFFFFFFFu, a[m], o);
-    }
-}
-
-// Accumulate the 64 codes of one 128-bit chunk against M activation rows.
-// xs points at column 64*q of activation row 0 in shared memory; rows are
-// `ldx` bf16 apart.
-template <int M>
-__device__ __forceinline__ void accumulate_chunk(const uint4 w4, const uint16_t *xs, int ldx,
-                                                 float (&acc)[M])
-{
-    const uint32_t words[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t w = words[i];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-#pragma unroll
-            for (int m = 0; m < M; ++m) {
-                const uint4 xv = *reinterpret_cast<const uint4 *>(xs + (size_t)m * ldx + 16 * i + 8 * h);
-                const uint32_t xp[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int code = 8 * h + 2 * j;
-                    acc[m] += sign_select(w >> (2 * code), bf16lo(xp[j]));
-                    acc[m] += sign_select(w >> (2 * (code + 1)), bf16hi(xp[j]));
-                }
-            }
-        }
-    }
-}
 
 // ---------------------------------------------------------------------------
 // Kernels
@@ -115,62 +47,52 @@ __global__ void k_unpack(const uint32_t *__restrict__ codes, int8_t *__restrict_
     reinterpret_cast<uint4 *>(t)[i] = make_uint4(out[0], out[1], out[2], out[3]);
 }
 
-// CUDA-core ternary GEMM for M activation rows (M = 1 is the GEMV).
-// Activations are staged once per CTA into shared memory as bf16 [M][k].
-// One warp per output row at a time; lane l handles 128-bit chunks
-// l, l+32, ... of the row.  With SWIGLU the same warp streams the gate row
-// and the up row and writes silu(g) * u.
-template <int M, bool SWIGLU>
-__global__ void __launch_bounds__(kCcThreads)
-k_gemm_cc(const uint32_t *__restrict__ cg, const float *__restrict__ sg,
-          const uint32_t *__restrict__ cu, const float *__restrict__ su,
-          const uint16_t *__restrict__ x, float *__restrict__ y, int rows, int k)
+// K == 0: every sum is empty, so y[i][r] = scale[r] * 0 and, for a SwiGLU
+// pair, h[i][r] = silu(scale_g[r] * 0) * (scale_u[r] * 0).  No weight is read.
+__global__ void k_empty_sum(const float *__restrict__ sg, const float *__restrict__ su, float *__restrict__ y,
+                            int rows, int m)
 {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    uint16_t *xs = reinterpret_cast<uint16_t *>(smem_raw);
-    const int nvec = (M * k) >> 3;  // 8 bf16 per 16-byte vector
-    for (int i = threadIdx.x; i < nvec; i += blockDim.x)
-        reinterpret_cast<uint4 *>(xs)[i] = reinterpret_cast<const uint4 *>(x)[i];
-    __syncthreads();
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int warps = blockDim.x >> 5;
-    const int64_t wpr = k >> 4;
-    const int chunks = k >> 6;
-    for (int r = blockIdx.x * warps + warp; r < rows; r += gridDim.x * warps) {
-        float ag[M], au[M];
-#pragma unroll
-        for (int m = 0; m < M; ++m) { ag[m] = 0.f; au[m] = 0.f; }
-        const uint4 *rg = reinterpret_cast<const uint4 *>(cg + (int64_t)r * wpr);
-        const uint4 *ru = SWIGLU ? reinterpret_cast<const uint4 *>(cu + (int64_t)r * wpr) : nullptr;
-        for (int q = lane; q < chunks; q += 32) {
-            const uint4 wg = ld_stream_u4(rg + q);
-            accumulate_chunk<M>(wg, xs + 64 * q, k, ag);
-            if constexpr (SWIGLU) {
-                const uint4 wu = ld_stream_u4(ru + q);
-                accumulate_chunk<M>(wu, xs + 64 * q, k, au);
-            }
-        }
-        warp_reduce<M>(ag);
-        if constexpr (SWIGLU) warp_reduce<M>(au);
-        if (lane == 0) {
-#pragma unroll
-            for (int m = 0; m < M; ++m) {
-                if constexpr (SWIGLU) {
-                    const float g = sg[r] * ag[m];
-                    const float u = su[r] * au[m];
-                    y[(int64_t)m * rows + r] = silu(g) * u;
-                } else {
-                    y[(int64_t)m * rows + r] = sg[r] * ag[m];
-                }
-            }
-        }
-    }
+    const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (int64_t)rows * m) return;
+    const int r = (int)(i % rows);
+    const float g = sg[r] * 0.0f;
+    y[i] = su == nullptr ? g : (g / (1.0f + expf(-g))) * (su[r] * 0.0f);
 }
 
 // ---------------------------------------------------------------------------
 // Launch helpers
 // ---------------------------------------------------------------------------
+
+// Driver entry points reached through the runtime (the library does not link
+// the driver library itself, so it also loads on a machine without one).
+template <typename F>
+static F driver_fn(const char *name)
+{
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<F>(p);
+}
+
+unsigned long long current_context_id()
+{
+    using GetCurrent = CUresult (*)(CUcontext *);
+    using GetId = CUresult (*)(CUcontext, unsigned long long *);
+    static const GetCurrent get_current = driver_fn<GetCurrent>("cuCtxGetCurrent");
+    static const GetId get_id = driver_fn<GetId>("cuCtxGetId");
+    if (get_current == nullptr || get_id == nullptr) return 0;
+    CUcontext c = nullptr;
+    if (get_current(&c) != CUDA_SUCCESS || c == nullptr) return 0;
+    unsigned long long id = 0;
+    if (get_id(c, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+static std::atomic<long long> g_wait_limit{mma::kWaitCycles};
+
+long long wait_limit() { return g_wait_limit.load(std::memory_order_relaxed); }
 
 int sm_count()
 {
@@ -182,50 +104,6 @@ int sm_count()
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
     if (dev >= 0 && dev < 64) cached[dev] = n;
     return n;
-}
-
-template <typename K>
-static cudaError_t allow_smem(K kernel, size_t bytes)
-{
-    if (bytes <= 48 * 1024) return cudaSuccess;
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-}
-
-template <int M, bool SWIGLU>
-static tern_status launch_cc(const tern_matrix *g, const tern_matrix *u, const uint16_t *x,
-                             float *y, cudaStream_t s)
-{
-    const int rows = g->rows, k = g->k;
-    const size_t smem = (size_t)M * k * sizeof(uint16_t);
-    auto kern = k_gemm_cc<M, SWIGLU>;
-    if (allow_smem(kern, smem) != cudaSuccess) return TERN_ERR_CUDA;
-    const int warps = kCcThreads / 32;
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kCcThreads, smem) != cudaSuccess || per_sm < 1)
-        per_sm = 1;
-    int64_t want = ((int64_t)rows + warps - 1) / warps;
-    int64_t cap = (int64_t)sm_count() * per_sm;
-    const int grid = (int)(want < cap ? want : cap);
-    kern<<<grid, kCcThreads, smem, s>>>(g->codes, g->scale, SWIGLU ? u->codes : nullptr,
-                                        SWIGLU ? u->scale : nullptr, x, y, rows, k);
-    return cudaGetLastError() == cudaSuccess ? TERN_OK : TERN_ERR_CUDA;
-}
-
-template <bool SWIGLU>
-static tern_status dispatch_cc(int m, const tern_matrix *g, const tern_matrix *u, const uint16_t *x,
-                               float *y, cudaStream_t s)
-{
-    switch (m) {
-    case 1: return launch_cc<1, SWIGLU>(g, u, x, y, s);
-    case 2: return launch_cc<2, SWIGLU>(g, u, x, y, s);
-    case 3: return launch_cc<3, SWIGLU>(g, u, x, y, s);
-    case 4: return launch_cc<4, SWIGLU>(g, u, x, y, s);
-    case 5: return launch_cc<5, SWIGLU>(g, u, x, y, s);
-    case 6: return launch_cc<6, SWIGLU>(g, u, x, y, s);
-    case 7: return launch_cc<7, SWIGLU>(g, u, x, y, s);
-    case 8: return launch_cc<8, SWIGLU>(g, u, x, y, s);
-    }
-    return TERN_ERR_M_RANGE;
 }
 
 // ---------------------------------------------------------------------------
@@ -264,6 +142,15 @@ tern_status check_gemm_args(const tern_matrix *g, const tern_matrix *u, const ui
     return TERN_OK;
 }
 
+// One product (a plain projection when u == nullptr, else a SwiGLU pair):
+// K == 0 has nothing to stream, everything else runs on the tensor cores.
+static tern_status run_product(const tern_matrix *g, const tern_matrix *u, const uint16_t *x, int m, float *y,
+                               cudaStream_t s)
+{
+    if (g->k == 0) return empty_sum(g, u, m, y, s);
+    return gemm_mma(g, u, x, m, y, s);
+}
+
 }  // namespace tern
 
 using namespace tern;
@@ -290,7 +177,7 @@ extern "C" tern_status tern_gemv(const tern_matrix *w, const uint16_t *x, float 
 {
     tern_status st = check_gemm_args(w, nullptr, x, 1, y);
     if (st != TERN_OK || w->rows == 0) return st;
-    return gemv_dispatch(w, x, y, (cudaStream_t)stream);
+    return run_product(w, nullptr, x, 1, y, (cudaStream_t)stream);
 }
 
 extern "C" tern_status tern_gemv_swiglu(const tern_matrix *gate, const tern_matrix *up,
@@ -299,7 +186,7 @@ extern "C" tern_status tern_gemv_swiglu(const tern_matrix *gate, const tern_matr
     if (up == nullptr) return TERN_ERR_NULL;
     tern_status st = check_gemm_args(gate, up, x, 1, h);
     if (st != TERN_OK || gate->rows == 0) return st;
-    return swiglu_dispatch(gate, up, x, 1, h, (cudaStream_t)stream);
+    return run_product(gate, up, x, 1, h, (cudaStream_t)stream);
 }
 
 extern "C" tern_status tern_gemm_smallm(const tern_matrix *w, const uint16_t *x, int32_t m,
@@ -307,7 +194,7 @@ extern "C" tern_status tern_gemm_smallm(const tern_matrix *w, const uint16_t *x,
 {
     tern_status st = check_gemm_args(w, nullptr, x, m, y);
     if (st != TERN_OK || w->rows == 0) return st;
-    return smallm_dispatch(w, x, m, y, (cudaStream_t)stream);
+    return run_product(w, nullptr, x, m, y, (cudaStream_t)stream);
 }
 
 extern "C" tern_status tern_gemm_smallm_swiglu(const tern_matrix *gate, const tern_matrix *up,
@@ -316,7 +203,7 @@ extern "C" tern_status tern_gemm_smallm_swiglu(const tern_matrix *gate, const te
     if (up == nullptr) return TERN_ERR_NULL;
     tern_status st = check_gemm_args(gate, up, x, m, h);
     if (st != TERN_OK || gate->rows == 0) return st;
-    return swiglu_dispatch(gate, up, x, m, h, (cudaStream_t)stream);
+    return run_product(gate, up, x, m, h, (cudaStream_t)stream);
 }
 
 // Checks every item of a batch as the single calls do.
@@ -337,7 +224,7 @@ extern "C" tern_status tern_gemm_batched(const tern_batch_item *items, int32_t n
 {
     const tern_status st = check_batch(items, n);
     if (st != TERN_OK || n == 0) return st;
-    return batched_dispatch(items, n, (cudaStream_t)stream);
+    return gemm_batched(items, n, (cudaStream_t)stream);
 }
 
 extern "C" tern_status tern_gemm_batched_noalloc(const tern_batch_item *items, int32_t n, void *stream)
@@ -357,6 +244,11 @@ extern "C" int32_t tern_gemm_batched_launches(const tern_batch_item *items, int3
     return batched_launches(items, n);
 }
 
+extern "C" void tern_set_wait_limit(int64_t cycles)
+{
+    g_wait_limit.store(cycles > 0 ? (long long)cycles : mma::kWaitCycles, std::memory_order_relaxed);
+}
+
 extern "C" tern_status tern_last_device_error(void *stream)
 {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return TERN_ERR_CUDA;
@@ -366,10 +258,21 @@ extern "C" tern_status tern_last_device_error(void *stream)
 
 namespace tern {
 
-tern_status gemm_cc(const tern_matrix *g, const tern_matrix *u, const uint16_t *x, int m, float *y,
-                    cudaStream_t s)
+tern_status empty_sum(const tern_matrix *g, const tern_matrix *u, int m, float *y, cudaStream_t s)
 {
-    return u ? dispatch_cc<true>(m, g, u, x, y, s) : dispatch_cc<false>(m, g, nullptr, x, y, s);
+    const int64_t n = (int64_t)g->rows * m;
+    if (n == 0) return TERN_OK;
+    const int threads = 256;
+    k_empty_sum<<<(unsigned)((n + threads - 1) / threads), threads, 0, s>>>(g->scale, u ? u->scale : nullptr, y,
+                                                                             g->rows, m);
+    return cudaGetLastError() == cudaSuccess ? TERN_OK : TERN_ERR_CUDA;
+}
+
+tern_status take_device_error()
+{
+    const tern_status a = take_mma_error();
+    const tern_status b = take_batched_error();
+    return a != TERN_OK ? a : b;
 }
 
 }  // namespace tern

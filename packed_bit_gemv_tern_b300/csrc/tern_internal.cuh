@@ -9,16 +9,21 @@
 
 namespace tern {
 
-constexpr int kCcThreads = 256;  // CUDA-core kernels: 8 warps per CTA
-
 int sm_count();
 tern_status check_matrix(const tern_matrix *w);
 
-// CUDA-core kernels (tern_cuda.cu); u == nullptr means a plain projection.
-tern_status gemm_cc(const tern_matrix *g, const tern_matrix *u, const uint16_t *x, int m, float *y,
-                    cudaStream_t s);
+// Unique id of the calling thread's current CUDA context, 0 if there is none
+// (keys per-context caches: a context made after a device reset is new).
+unsigned long long current_context_id();
 
-// Tensor-core kernels (tern_mma.cu); same contract as gemm_cc.
+// Bound of the kernels' mbarrier waits, in SM cycles, passed to every launch
+// (tern_set_wait_limit; kWaitCycles by default).
+long long wait_limit();
+
+// K == 0 products (tern_cuda.cu): y = scale * 0 (a SwiGLU pair when u != nullptr).
+tern_status empty_sum(const tern_matrix *g, const tern_matrix *u, int m, float *y, cudaStream_t s);
+
+// Tensor-core kernels (tern_mma.cu); u == nullptr means a plain projection.
 tern_status gemm_mma(const tern_matrix *g, const tern_matrix *u, const uint16_t *x, int m, float *y,
                      cudaStream_t s);
 tern_status take_mma_error();
@@ -36,13 +41,6 @@ tern_status take_batched_error();
 // Shared argument checks (tern_cuda.cu).
 tern_status check_gemm_args(const tern_matrix *g, const tern_matrix *u, const uint16_t *x, int32_t m,
                             const float *y);
-
-// Kernel choice per entry point (tern_dispatch.cu).
-tern_status gemv_dispatch(const tern_matrix *w, const uint16_t *x, float *y, cudaStream_t s);
-tern_status swiglu_dispatch(const tern_matrix *g, const tern_matrix *u, const uint16_t *x, int m,
-                            float *h, cudaStream_t s);
-tern_status smallm_dispatch(const tern_matrix *w, const uint16_t *x, int m, float *y, cudaStream_t s);
-tern_status batched_dispatch(const tern_batch_item *items, int n, cudaStream_t s);
 
 // Reads and clears every device error word (TERN_OK when all are clear).
 tern_status take_device_error();

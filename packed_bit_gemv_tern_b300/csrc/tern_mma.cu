@@ -15,13 +15,17 @@
 //     requested before anything waits on it (programmatic dependent launch).
 //   * warps 1-4: B operand staging.  After griddepcontrol.wait they turn the
 //     activations of the K range into the MMA's B operand.  Each bf16 value x
-//     of activation row m is split into two e4m3 terms under a per-row
-//     power-of-two scale 2^s (the row's largest |x| lands in [128, 256)):
+//     of activation row i goes to one of two magnitude bands.  Band A holds
+//     the elements with |x| >= 2^(e-13), where 2^e <= max|x| < 2^(e+1) over
+//     the row; band B the others, with 2^f <= max over band B < 2^(f+1).  In
+//     its band, x is split into two e4m3 terms under the band's power-of-two
+//     scale 2^s (the band maximum lands in [128, 256)):
 //     x*2^s = hi + lo/16, hi = RN_e4m3(x*2^s), lo = RN_e4m3((x*2^s - hi)*16).
-//     A bf16 value has 8 significant bits and each e4m3 term holds 4, so with
-//     2^e <= max|x| < 2^(e+1) the split is exact for every |x| >= 2^(e-13);
-//     smaller elements carry an absolute error of at most 2^(e-21).  Column 2m
-//     of B holds hi, 2m+1 lo (N = 16 covers M <= 8).
+//     A bf16 value has 8 significant bits and each e4m3 term holds 4, so a
+//     band's split is exact for every element at least 2^-13 of its band
+//     maximum: band A always, band B for |x| >= 2^(f-13); smaller elements
+//     carry an absolute error of at most 2^(f-21).  B rows 4i .. 4i+3 hold
+//     hi_A, lo_A, hi_B, lo_B of row i (N = 16 for m <= 4, 32 above).
 //   * warps 5-12: two decoder warpgroups taking alternate chunks of 8 words
 //     (128 codes) per row.  Thread i owns weight row i (TMEM lane i).  Each
 //     32-bit word (16 codes) becomes four registers of four e4m3 bytes:
@@ -31,12 +35,13 @@
 //     a weight.  The 32 registers go to the chunk's TMEM slot (tcgen05.st);
 //     the group's four warps meet at a named barrier, then warp q issues the
 //     chunk's K=32 step q (tcgen05.mma kind::f8f6f4, A e4m3 from TMEM, B e4m3
-//     from shared memory, M = 128, N = 16) into its own fp32 accumulator
-//     D[g][q] and commits the slot back.  Spreading the issue over eight warps
+//     from shared memory, M = 128, N = 16 or 32) into its own fp32
+//     accumulator D[q] and commits the slot back.  Spreading the issue over eight warps
 //     keeps the per-thread issue cost (about 45 cycles per MMA) off the
 //     critical path.
-//   * epilogue: the eight accumulators are summed (tcgen05.ld), hi/lo columns
-//     rescaled by 2^-s and 2^-(s+4), split-K partials pushed into rank 0's
+//   * epilogue: the four accumulators are summed (tcgen05.ld), the hi/lo
+//     columns of each band rescaled by 2^-s and 2^-(s+4), split-K partials
+//     pushed into rank 0's
 //     shared memory and summed there in rank order after one cluster barrier,
 //     then y = scale * (0.5 * sum) (the weights entered as +-2), or
 //     silu(gate) * up for the SwiGLU pair (tile rows 0-63 are gate rows,
@@ -70,7 +75,7 @@ constexpr int kFirstDecWarp = 1 + kStagerWarps;  // warps 5-12: decoders (two wa
 constexpr int kChunkWords = 8;            // words per row per decode chunk (2 x 16 B)
 constexpr int kASlots = 3;                // TMEM A slots, one stage (128 columns) each
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kDCol = kASlots * 128;  // accumulators D[k], k < kIssuers, at [kDCol, kDCol + 16 kIssuers)
+constexpr uint32_t kDCol = kASlots * 128;  // accumulators D[k], k < kIssuers, at kDCol + N k
 constexpr int kMaxWStages = 8;
 // Every CTA allocates all 512 TMEM columns.  Asking for more than half of the
 // SM's shared memory keeps one CTA per SM, so tcgen05.alloc never waits for a
@@ -92,6 +97,7 @@ struct MmaParams {
     int per_st;       // stages per cluster rank
     int split;        // cluster size
     int n_wst;        // shared-memory weight ring depth
+    long long wait_limit;  // bound of every Waiter, in cycles
     uint32_t off_b;   // shared-memory byte offsets from the 1024-aligned base
     uint32_t off_red;
     uint32_t off_xch;
@@ -106,8 +112,12 @@ constexpr uint32_t kBarAEmpty = kBarAFull + 8 * kASlots;            // [kASlots]
 constexpr uint32_t kBarBReady = kBarAEmpty + 8 * kASlots;
 constexpr uint32_t kBarDFull = kBarBReady + 8;                      // one arrival per issuer
 constexpr uint32_t kWords = kBarDFull + 8;                          // uint32 scratch after barriers
-// words: [0] tmem base, [1] abort, [2] bit mask of written accumulators, [4..11] max|x| bits per row
-constexpr uint32_t kBarBytes = kWords + 16 * 4;
+// words: [0] tmem base, [1] abort, [2] bit mask of written accumulators,
+// [3] band count, [4 + 2i] max|x| bits of activation row i, [5 + 2i] its
+// band-B maximum, [20 + i] its count of nonzero elements below the band
+// threshold, [28 + i] its sum of |x| (fp32)
+constexpr uint32_t kWordsCount = 40;
+constexpr uint32_t kBarBytes = kWords + kWordsCount * 4;
 
 using namespace mma;
 
@@ -122,12 +132,14 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
 
     const uint32_t wbuf = base;
     const uint32_t bbuf = base + p.off_b;
-    float *red = reinterpret_cast<float *>(gbase + p.off_red);   // [split][128][8]
+    float *red = reinterpret_cast<float *>(gbase + p.off_red);   // [split][128][16]: pair (hi[8], lo[8]) per row
     float *xch = reinterpret_cast<float *>(gbase + p.off_xch);   // [64][8]
     const uint32_t bars = base + p.off_bar;
     uint32_t *words = reinterpret_cast<uint32_t *>(gbase + p.off_bar + kWords);
     volatile uint32_t *abort_flag = words + 1;
-    uint32_t *xmax = words + 4;  // [8] max |x| (fp32 bits) per activation row
+    uint32_t *xmax = words + 4;  // [2i], [2i + 1]: max |x| and band-B max (fp32 bits) of activation row i
+    uint32_t *n_small = words + 20;
+    float *sum_abs = reinterpret_cast<float *>(words + 28);
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
@@ -169,7 +181,7 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
         }
         ptx::mbar_init(bars + kBarBReady, kStagers);
         ptx::mbar_init(bars + kBarDFull, kIssuers);
-        for (int j = 1; j < 16; ++j) words[j] = 0u;
+        for (int j = 1; j < (int)kWordsCount; ++j) words[j] = 0u;
         ptx::fence_proxy_async_smem();
         if (n_st > 0) {
             ptx::prefetch_tmap(&tm_g);
@@ -187,7 +199,7 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
     ptx::tc_fence_after();
     const uint32_t tmem = words[0];
     if (tid == 0) ptx::grid_dep_launch();
-    const Waiter waiter{abort_flag, &g_mma_error};
+    const Waiter waiter(abort_flag, &g_mma_error, p.wait_limit);
 
     if (warp == 0) {
         // ----------------------------------------------------------- producer
@@ -213,7 +225,7 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
         // Items are processed in batches of kStageItems per thread: all loads of
         // a batch are issued before any is used, so a batch costs one memory
         // latency.  Small problems (n_items <= kStagers * kStageItems) keep
-        // their activations in registers between the max pass and the split.
+        // their activations in registers across the three passes.
         constexpr int kStageItems = 4;
         uint4 xa[kStageItems], xb[kStageItems];
         const bool resident = n_items <= kStagers * kStageItems;
@@ -239,10 +251,33 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
 #pragma unroll
             for (int t = 0; t < kStageItems; ++t) {
                 const int item = first + t * kStagers;
-                if (item < n_items) atomicMax(&xmax[item / n_words], max_abs16(xa[t], xb[t]));
+                if (item < n_items) atomicMax(&xmax[2 * (item / n_words)], max_abs16(xa[t], xb[t]));
             }
         }
         ptx::named_bar_sync(3, kStagers);
+        for (int first = st_tid; first < n_items; first += kStagers * kStageItems) {  // band B of each row
+            if (!resident) load_batch(first);
+#pragma unroll
+            for (int t = 0; t < kStageItems; ++t) {
+                const int item = first + t * kStagers;
+                if (item < n_items) {
+                    const int mm = item / n_words;
+                    const uint32_t tb2 = band_threshold2(xmax[2 * mm]);
+                    uint32_t n = 0;
+                    float sabs = 0.f;
+                    band_stats16(xa[t], xb[t], tb2, n, sabs);
+                    atomicMax(&xmax[2 * mm + 1], max_abs16_below(xa[t], xb[t], tb2));
+                    atomicAdd(&n_small[mm], n);
+                    atomicAdd(&sum_abs[mm], sabs);
+                }
+            }
+        }
+        ptx::named_bar_sync(3, kStagers);
+        // one or two bands for every row of this CTA's K range (need_two_bands)
+        if (st_tid < m && need_two_bands(xmax[2 * st_tid], n_small[st_tid], sum_abs[st_tid])) atomicOr(&words[3], 1u);
+        ptx::named_bar_sync(3, kStagers);
+        const int bands = words[3] != 0u ? 2 : 1;
+        const uint32_t wbytes = b_block_bytes(m, bands);
         for (int first = st_tid; first < n_items; first += kStagers * kStageItems) {  // e4m3 pieces
             if (!resident) load_batch(first);
 #pragma unroll
@@ -250,19 +285,21 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
                 const int item = first + t * kStagers;
                 if (item >= n_items) break;
                 const int mm = item / n_words, wi = item - mm * n_words;
-                uint4 hi4 = make_uint4(0, 0, 0, 0), lo4 = make_uint4(0, 0, 0, 0);
-                if (k0 + 16 * wi < p.k) split_word(xa[t], xb[t], exp2i(row_scale_exp(xmax[mm])), hi4, lo4);
-                const uint32_t at = bbuf + (uint32_t)wi * kBBytesPerWord;
-                ptx::sts128(at + b_row_off(2 * mm), hi4);
-                ptx::sts128(at + b_row_off(2 * mm + 1), lo4);
+                const uint32_t at = bbuf + (uint32_t)wi * wbytes + 32u * (uint32_t)(bands * mm);
+                const float sca = exp2i(row_scale_exp(xmax[2 * mm]));
+                if (bands == 2) {
+                    uint4 rows[4];
+                    split_word2(xa[t], xb[t], sca, exp2i(row_scale_exp(xmax[2 * mm + 1])), band_threshold2(xmax[2 * mm]),
+                                rows);
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) ptx::sts128(at + 16u * (uint32_t)r, rows[r]);
+                } else {
+                    uint4 rows[2];
+                    split_word1(xa[t], xb[t], sca, rows);
+                    ptx::sts128(at, rows[0]);
+                    ptx::sts128(at + 16u, rows[1]);
+                }
             }
-        }
-        // rows n >= 2m of B are zero
-        for (int item = st_tid; item < (8 - m) * n_words; item += kStagers) {
-            const int mm = m + item / n_words, wi = item % n_words;
-            const uint32_t at = bbuf + (uint32_t)wi * kBBytesPerWord;
-            ptx::sts128(at + b_row_off(2 * mm), make_uint4(0, 0, 0, 0));
-            ptx::sts128(at + b_row_off(2 * mm + 1), make_uint4(0, 0, 0, 0));
         }
         ptx::fence_proxy_async_smem();
         ptx::mbar_arrive(bars + kBarBReady);
@@ -270,9 +307,11 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
         // Issuer k takes the K=32 steps 4k..4k+3 of every stage (16 steps of
         // two words each) into its own accumulator D[k].
         const int k_iss = warp - 1;
+        const int n_mma = mma_n(m, bands);
+        const uint32_t idesc = idesc_n(n_mma);
         if (lane == 0) {
             bool ok = waiter.wait(bars + kBarBReady, 0);  // all staging warps are done
-            const uint32_t d = tmem + kDCol + 16u * (uint32_t)k_iss;
+            const uint32_t d = tmem + kDCol + (uint32_t)(n_mma * k_iss);
             for (int st = 0; st < n_st && ok; ++st) {
                 const int slot = st % kASlots;
                 if (!waiter.wait(bars + kBarAFull + 8 * slot, (st / kASlots) & 1)) break;
@@ -282,7 +321,7 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
                     const int step = 4 * k_iss + t;               // K=32 step within the stage
                     const int wi = st * kStageWords + 2 * step;   // its first word
                     ptx::mma_ts_f8f6f4(d, tmem + (uint32_t)(slot * 128 + step * 8),
-                                       b_desc(bbuf + (uint32_t)wi * kBBytesPerWord), kIdesc,
+                                       b_desc_lbo(bbuf + (uint32_t)wi * wbytes, wbytes), idesc,
                                        (st | t) != 0 ? 1u : 0u);
                 }
                 ptx::mma_commit(bars + kBarAEmpty + 8 * slot);
@@ -334,33 +373,67 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
     // the epilogue reads them.
     __syncwarp();
     __syncthreads();
-    float acc[8];
+    // per activation row, this rank's sum as an unevaluated pair (acc_pair):
+    // its bands, and then the ranks' partials, may cancel at very different
+    // magnitudes
+    float acc[8], acc_lo[8];
 #pragma unroll
-    for (int n = 0; n < 8; ++n) acc[n] = 0.f;
+    for (int n = 0; n < 8; ++n) acc[n] = acc_lo[n] = 0.f;
     const bool epi = (warp >= kFirstDecWarp && warp < kFirstDecWarp + 4);  // warpgroup 0 reads D
     const int quad = warp & 3;
     const int i = quad * 32 + lane;
     if (epi && n_chunks > 0) {
-        float dsum[16];
-#pragma unroll
-        for (int n = 0; n < 16; ++n) dsum[n] = 0.f;
+        const int bands = words[3] != 0u ? 2 : 1;
+        const int n_mma = mma_n(m, bands);
         if (waiter.wait(bars + kBarDFull, 0)) {
             ptx::tc_fence_after();
             const uint32_t written = words[2];
-            for (int a = 0; a < kIssuers; ++a) {
-                if (!((written >> a) & 1u)) continue;
-                uint32_t d[16];
-                ptx::tmem_ld_32x32b_x16(tmem + ((uint32_t)(quad * 32) << 16) + kDCol + 16u * a, d);
-                ptx::tmem_wait_ld();
+            const uint32_t lane_base = tmem + ((uint32_t)(quad * 32) << 16) + kDCol;
+            // Sums the 16-column group at `col` of every written accumulator
+            // (the same bands and scales: plain fp32 adds).
+            auto sum_group = [&](uint32_t col, float (&dsum)[16]) {
 #pragma unroll
-                for (int n = 0; n < 16; ++n) dsum[n] += __uint_as_float(d[n]);
-            }
-        }
+                for (int q = 0; q < 16; ++q) dsum[q] = 0.f;
+                for (int a = 0; a < kIssuers; ++a) {
+                    if (!((written >> a) & 1u)) continue;
+                    uint32_t d[16];
+                    ptx::tmem_ld_32x32b_x16(lane_base + (uint32_t)(n_mma * a) + col, d);
+                    ptx::tmem_wait_ld();
 #pragma unroll
-        for (int mm = 0; mm < 8; ++mm) {
-            if (mm < m) {
-                const int s = row_scale_exp(xmax[mm]);
-                acc[mm] = dsum[2 * mm] * exp2i(-s) + dsum[2 * mm + 1] * exp2i(max(-s - 4, -126));
+                    for (int q = 0; q < 16; ++q) dsum[q] += __uint_as_float(d[q]);
+                }
+            };
+            // each row's band terms, at their scales (hi 2^-s, lo 2^-(s+4)
+            // of each band), go into its pair
+            if (bands == 1) {  // column 2i + b of row i: hi, lo
+                float dsum[16];
+                sum_group(0u, dsum);
+#pragma unroll
+                for (int mm = 0; mm < 8; ++mm) {
+                    if (mm < m) {
+                        const int sa = row_scale_exp(xmax[2 * mm]);
+                        acc_pair(acc[mm], acc_lo[mm], dsum[2 * mm] * exp2i(-sa));
+                        acc_pair(acc[mm], acc_lo[mm], dsum[2 * mm + 1] * exp2i(-sa - 4));
+                    }
+                }
+            } else {  // column 4i + b of row i: hi_A, lo_A, hi_B, lo_B
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    if (4 * h >= m) break;
+                    float dsum[16];
+                    sum_group(16u * (uint32_t)h, dsum);
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int mm = 4 * h + r;
+                        if (mm < m) {
+                            const int sa = row_scale_exp(xmax[2 * mm]), sb = row_scale_exp(xmax[2 * mm + 1]);
+                            acc_pair(acc[mm], acc_lo[mm], dsum[4 * r] * exp2i(-sa));
+                            acc_pair(acc[mm], acc_lo[mm], dsum[4 * r + 1] * exp2i(-sa - 4));
+                            acc_pair(acc[mm], acc_lo[mm], dsum[4 * r + 2] * exp2i(-sb));
+                            acc_pair(acc[mm], acc_lo[mm], dsum[4 * r + 3] * exp2i(-sb - 4));
+                        }
+                    }
+                }
             }
         }
     }
@@ -369,23 +442,29 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
         // every rank pushes its partial into rank 0's buffer slot [rank]; one
         // cluster barrier; rank 0 sums the slots in rank order
         if (epi) {
-            const uint32_t dst = ptx::mapa(ptx::smem_u32(red + ((size_t)rank * 128 + i) * 8), 0u);
+            const uint32_t dst = ptx::mapa(ptx::smem_u32(red + ((size_t)rank * 128 + i) * 16), 0u);
             ptx::st_cluster_v4(dst, acc[0], acc[1], acc[2], acc[3]);
             ptx::st_cluster_v4(dst + 16u, acc[4], acc[5], acc[6], acc[7]);
+            ptx::st_cluster_v4(dst + 32u, acc_lo[0], acc_lo[1], acc_lo[2], acc_lo[3]);
+            ptx::st_cluster_v4(dst + 48u, acc_lo[4], acc_lo[5], acc_lo[6], acc_lo[7]);
         }
         ptx::cluster_arrive();
         ptx::cluster_wait();
         if (epi && rank == 0) {
 #pragma unroll
-            for (int n = 0; n < 8; ++n) acc[n] = 0.f;
+            for (int n = 0; n < 8; ++n) acc[n] = acc_lo[n] = 0.f;
             for (int r = 0; r < split; ++r) {
-                const float4 a = *reinterpret_cast<const float4 *>(red + ((size_t)r * 128 + i) * 8);
-                const float4 b = *reinterpret_cast<const float4 *>(red + ((size_t)r * 128 + i) * 8 + 4);
-                acc[0] += a.x; acc[1] += a.y; acc[2] += a.z; acc[3] += a.w;
-                acc[4] += b.x; acc[5] += b.y; acc[6] += b.z; acc[7] += b.w;
+                const float *v = red + ((size_t)r * 128 + i) * 16;
+#pragma unroll
+                for (int n = 0; n < 8; ++n) {
+                    acc_pair(acc[n], acc_lo[n], v[n]);
+                    acc_pair(acc[n], acc_lo[n], v[8 + n]);
+                }
             }
         }
     }
+#pragma unroll
+    for (int n = 0; n < 8; ++n) acc[n] = __fadd_rn(acc[n], acc_lo[n]);
     if (rank == 0 && epi) {
         if constexpr (SWIGLU) {
             const int r = row0 + (i & 63);
@@ -440,11 +519,13 @@ tern_status launch_mma(const tern_matrix *g, const tern_matrix *u, const uint16_
 
     int split = 1;
     while (split < 8 && tiles * split * 2 <= sms && split * 2 <= total_st) split *= 2;
-    const uint32_t misc = 8 * 128 * 8 * 4 + 64 * 8 * 4 + kBarBytes + 64;
+    const uint32_t wbytes = b_block_bytes(m, 2);  // room for two bands
     int per_st = 0, n_wst = 0;
     for (;;) {
         per_st = total_st > 0 ? (total_st + split - 1) / split : 0;
-        const uint32_t fixed = 1024 + (uint32_t)per_st * kStageWords * kBBytesPerWord + misc;
+        // split-K partials (a pair of 8 per row per rank), SwiGLU exchange, barriers
+        const uint32_t misc = (uint32_t)split * 128 * 16 * 4 + 64 * 8 * 4 + kBarBytes + 64;
+        const uint32_t fixed = 1024 + (uint32_t)per_st * kStageWords * wbytes + kBPad + misc;
         n_wst = fixed < (uint32_t)kSmemLimit ? (int)((kSmemLimit - fixed) / kStageBytes) : 0;
         if (n_wst > kMaxWStages) n_wst = kMaxWStages;
         if (n_wst > per_st && per_st >= 1) n_wst = per_st < 2 ? 2 : per_st;  // no deeper than the work
@@ -469,9 +550,10 @@ tern_status launch_mma(const tern_matrix *g, const tern_matrix *u, const uint16_
     prm.per_st = per_st;
     prm.split = split;
     prm.n_wst = n_wst;
+    prm.wait_limit = wait_limit();
     prm.off_b = (uint32_t)n_wst * kStageBytes;
-    prm.off_red = prm.off_b + (uint32_t)per_st * kStageWords * kBBytesPerWord;
-    prm.off_xch = prm.off_red + (uint32_t)split * 128 * 8 * 4;
+    prm.off_red = prm.off_b + (uint32_t)per_st * kStageWords * wbytes + kBPad;
+    prm.off_xch = prm.off_red + (uint32_t)split * 128 * 16 * 4;
     prm.off_bar = prm.off_xch + 64 * 8 * 4;
     uint32_t smem = 1024 + prm.off_bar + kBarBytes;
     if (smem < kMinSmem) smem = kMinSmem;

@@ -84,6 +84,34 @@ def activations(rng: np.random.Generator, m: int, k: int) -> np.ndarray:
     return f32_to_bf16_bits(rng.standard_normal((m, k), dtype=np.float32))
 
 
+def outlier_activations(rng: np.random.Generator, m: int, k: int, magnitude: float,
+                        n_outliers: int = 3, shared_channels: bool = False) -> np.ndarray:
+    """bf16 bits [m, k]: N(0, 1) samples with ``n_outliers`` channels per row
+    replaced by +-``magnitude`` (random sign).
+
+    Decoder activations carry a few channels far above the rest; these rows
+    put the row maximum ``magnitude`` above a bulk of unit scale.  With
+    ``shared_channels`` every row uses the same outlier channels (fixed
+    outlier dimensions), otherwise each row draws its own.
+    """
+    x = rng.standard_normal((m, k), dtype=np.float32)
+    n = min(n_outliers, k)
+    shared = rng.choice(k, size=n, replace=False)
+    for i in range(m):
+        ch = shared if shared_channels else rng.choice(k, size=n, replace=False)
+        x[i, ch] = np.where(rng.random(n) < 0.5, -1.0, 1.0).astype(np.float32) * np.float32(magnitude)
+    return f32_to_bf16_bits(x)
+
+
+def far_bulk_activations(rng: np.random.Generator, m: int, k: int, bulk_log2: int) -> np.ndarray:
+    """bf16 bits [m, k]: a bulk of N(0, 1) * 2**bulk_log2 with one element per
+    row of magnitude 1 (the row maximum sits far above everything else)."""
+    x = rng.standard_normal((m, k), dtype=np.float32) * np.float32(2.0 ** bulk_log2)
+    for i in range(m):
+        x[i, rng.integers(0, k)] = np.float32(1.0 if rng.random() < 0.5 else -1.0)
+    return f32_to_bf16_bits(x)
+
+
 def small_int_activations(rng: np.random.Generator, m: int, k: int,
                           lo: int = -2, hi: int = 2) -> np.ndarray:
     """bf16 bits [m, k] of integers in [lo, hi] (exact in bf16).

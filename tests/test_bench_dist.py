@@ -60,7 +60,8 @@ def test_single_rank_needs_no_group():
 
 def test_persistent_launch_count():
     """bench.py's roofline divides by the persistent kernel's launches only:
-    a group with m >= 2 items adds a preparing launch to the full count."""
+    a group with m >= 2 items adds a preparing launch to the full count, and
+    an item with k == 0 a small launch of its own."""
     import ctypes
 
     sys.path.insert(0, ROOT)
@@ -70,10 +71,14 @@ def test_persistent_launch_count():
     build.build()
     tern.load()
     w = tern.CMatrix(4096, 4096, 0x1000, 0x2000, None)
-    for m, n, total, main in ((1, 100, 1, 1), (7, 8, 2, 1), (7, 200, 4, 2), (2, 1, 2, 1)):
+    w0 = tern.CMatrix(8, 0, 0x1000, 0x2000, None)
+    for m, n, k_zero, total, main in ((1, 100, 0, 1, 1), (7, 8, 0, 2, 1), (7, 200, 0, 4, 2), (2, 1, 0, 2, 1),
+                                      (1, 3, 2, 3, 1), (7, 3, 2, 4, 1)):
         arr = (tern.CBatchItem * n)()
         for i in range(n):
             arr[i].w, arr[i].x, arr[i].y, arr[i].m = ctypes.addressof(w), 0x3000, 0x4000, m
+        for i in range(1, 1 + k_zero):  # items with k == 0 beside the real ones
+            arr[i].w = ctypes.addressof(w0)
         assert tern.tern_gemm_batched_launches(arr) == total
         assert bench.persistent_launches(arr) == main
         assert [it.m for it in arr] == [m] * n  # the caller's array is untouched

@@ -131,7 +131,7 @@ def test_swiglu_matches_oracle(rows, k):
     _guard_ok(full, 1, rows)
 
 
-@pytest.mark.parametrize("m", [1, 2, 3, 5, 7, 8])
+@pytest.mark.parametrize("m", [1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("rows,k", [(33, 192), (1024, 4096), (300, 12288)])
 def test_smallm_matches_oracle(m, rows, k):
     rng = np.random.default_rng(m * 1000 + rows + k)
@@ -223,7 +223,7 @@ def test_side_stream_and_reuse():
 def _run_step(wl, api):
     """One step of a workload: through tern_gemm_batched as bench.py times it by
     default (one persistent launch per group, after an activation-preparing
-    launch when items have m >= 2), or one tern_* call per linear."""
+    launch), or one tern_* call per linear."""
     if api == "batched":
         workloads.run_batched(workloads.batch_of(wl.calls))
     else:
@@ -304,6 +304,22 @@ def test_batched_mixed_items():
         _guard_ok(full, m, rows)
 
 
+def test_batched_one_stage_chunks_in_one_cta():
+    """A CTA whose run is three one-stage tiles of one item (257 x 320) ahead
+    of a SwiGLU pair: the issuers of a later tile reach their waits while the
+    staging warps still build the first tile's operand, so every buffer wait
+    must be for the right phase (a parity wait issued a phase early returns
+    at once).  Run three times; every element against the oracle."""
+    rng = np.random.default_rng(409)
+    for _ in range(3):
+        made = [_item(rng, 257, 320, 1), _item(rng, 640, 4096, 1, swiglu=True)]
+        tern.tern_gemm_batched([mi[0] for mi in made])
+        torch.cuda.synchronize()
+        assert tern.tern_last_device_error() == tern.TERN_OK
+        for it, ref, full in made:
+            _close(it[3].cpu().numpy(), ref, "one-stage chunks")
+
+
 def test_batched_exact_integers_and_many_items():
     """More items than one launch carries (split over several launches),
     integer activations: every result bit-exact."""
@@ -311,7 +327,6 @@ def test_batched_exact_integers_and_many_items():
     made = [_item(rng, 128 + 64 * (i % 5), 4096 if i % 3 else 12288, 1 + (i % 8), swiglu=(i % 4 == 0), int_x=True)
             for i in range(150)]
     # two persistent launches, each after an activation-preparing launch
-    # (both groups hold items with m >= 2)
     assert tern.tern_gemm_batched_launches([mi[0] for mi in made]) == 4
     tern.tern_gemm_batched([mi[0] for mi in made])
     torch.cuda.synchronize()

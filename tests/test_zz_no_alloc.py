@@ -1,8 +1,14 @@
 """tern_gemm_batched_noalloc against the existing tern_gemm_batched: the same
 bytes for the same batch over two calls in a row (with new activations for
-the second, so stale scratch would show), and an oversize batch rejected
+the second, so stale scratch would show), a batch whose two launch groups
+both prepare activations in the one array, and an oversize batch rejected
 before anything runs.  The file is named to be collected last: it must pass
-both alone and after every other test in one process."""
+both alone and after every other test in one process.
+
+Callers that cannot allocate device memory (a serving engine that has
+reserved the GPU's memory for its own pools, code that may not call
+cudaMalloc) use the no-alloc entry point; these tests hold it to the
+allocating one, bit for bit."""
 import ctypes
 
 import numpy as np
@@ -65,6 +71,50 @@ def test_noalloc_matches_batched_over_two_calls():
 
 
 @pytest.mark.gpu
+def test_noalloc_two_launch_groups_share_the_array():
+    """130 small items with m >= 2 take two launch groups, and each group's
+    activation-preparing launch writes the array from offset 0: the second
+    must not overwrite it while the first group's persistent kernel still
+    reads it.  Two calls in a row, compared bit for bit with
+    tern_gemm_batched, which is itself checked against the oracle."""
+    import oracle
+    rng = np.random.default_rng(2026)
+    specs = [(64 + 32 * (i % 4), 64 * (1 + i % 8), 2 + i % 7) for i in range(130)]
+    ws, cs = [], []
+    for rows, k, m in specs:
+        t = synth.ternary(rng, rows, k)
+        codes, rowsum = tern.tern_pack(t)
+        sc = synth.scales(rng, rows)
+        ws.append(tern.TernMatrix.from_host(codes, sc, k, rowsum))
+        cs.append((codes, sc))
+
+    def xs():
+        return [synth.activations(rng, m, k) for rows, k, m in specs]
+
+    def run(fn, xb):
+        ys = [torch.full((m, rows), float("nan"), dtype=torch.float32, device="cuda") for rows, k, m in specs]
+        items = [(w, None, torch.from_numpy(x.view(np.int16)).cuda().view(torch.bfloat16), y, m)
+                 for w, x, y, (rows, k, m) in zip(ws, xb, ys, specs)]
+        assert tern.tern_gemm_batched_launches(items) == 4  # two groups, each with a preparing launch
+        fn(items)
+        torch.cuda.synchronize()
+        assert tern.tern_last_device_error() == tern.TERN_OK
+        return ys
+
+    xa, xb = xs(), xs()
+    ref_a, ref_b = run(tern.tern_gemm_batched, xa), run(tern.tern_gemm_batched, xb)
+    got_a, got_b = run(tern.tern_gemm_batched_noalloc, xa), run(tern.tern_gemm_batched_noalloc, xb)
+    for i, (rows, k, m) in enumerate(specs):
+        assert torch.equal(got_a[i].view(torch.int32), ref_a[i].view(torch.int32)), ("first call", i)
+        assert torch.equal(got_b[i].view(torch.int32), ref_b[i].view(torch.int32)), ("second call", i)
+    for i in (0, 63, 64, 65, 129):  # items on both sides of the group boundary
+        codes, sc = cs[i]
+        ref = oracle.gemm(codes, sc, specs[i][1], xb[i], threads=4)
+        got = got_b[i].cpu().numpy().astype(np.float64)
+        assert (np.abs(got - ref) <= np.maximum(1e-3 * np.abs(ref), 1e-4)).all(), i
+
+
+@pytest.mark.gpu
 def test_noalloc_oversize_launches_nothing():
     rng = np.random.default_rng(2025)
     t = synth.ternary(rng, 64, 12288)
@@ -81,7 +131,7 @@ def test_noalloc_oversize_launches_nothing():
 
 def test_noalloc_size_check_on_host():
     """The scratch limit is enforced before any CUDA call (fake pointers,
-    never dereferenced): 24 items of m = 8, k = 12288 need about 4.7 MB."""
+    never dereferenced): 24 items of m = 8, k = 12288 need about 9.4 MB."""
     from packed_bit_gemv_tern_b300 import build
     build.build()
     lib = tern.load()
