@@ -232,7 +232,7 @@ struct PrepParams {
     PrepItem item[kMaxItems];
 };
 
-// Maximum (or sum) of v over the CTA of k_tern_bprep; every thread gets it.
+// Maximum of v over the CTA of k_tern_bprep; every thread gets it.
 __device__ __forceinline__ uint32_t prep_cta_max(uint32_t v, uint32_t *red)
 {
     v = __reduce_max_sync(0xFFFFFFFFu, v);
@@ -244,34 +244,10 @@ __device__ __forceinline__ uint32_t prep_cta_max(uint32_t v, uint32_t *red)
     return v;
 }
 
-__device__ __forceinline__ uint32_t prep_cta_add(uint32_t v, uint32_t *red)
-{
-    v = __reduce_add_sync(0xFFFFFFFFu, v);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    v = 0;
-#pragma unroll
-    for (int w = 0; w < kPrepThreads / 32; ++w) v += red[w];
-    __syncthreads();
-    return v;
-}
-
-__device__ __forceinline__ float prep_cta_addf(float v, float *red)
-{
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    v = 0.f;
-#pragma unroll
-    for (int w = 0; w < kPrepThreads / 32; ++w) v += red[w];
-    __syncthreads();
-    return v;
-}
-
 __global__ void __launch_bounds__(kPrepThreads) k_tern_bprep(const __grid_constant__ PrepParams p)
 {
     __shared__ uint32_t red[kPrepThreads / 32];
+    __shared__ uint32_t stat[kPrepThreads / 32][3];
     // The persistent kernel that follows may start at once: its weight stream
     // needs nothing from here, and its staging warps wait for this grid to
     // finish before they read the workspace.  The previous kernel on the
@@ -310,9 +286,25 @@ __global__ void __launch_bounds__(kPrepThreads) k_tern_bprep(const __grid_consta
         band_stats16(va[q], vb[q], tb2, n, sabs);
         mb = max(mb, max_abs16_below(va[q], vb[q], tb2));
     }
-    mb = prep_cta_max(mb, red);
-    n = prep_cta_add(n, red);
-    sabs = prep_cta_addf(sabs, reinterpret_cast<float *>(red));
+    // the three statistics over the CTA in one round
+    mb = __reduce_max_sync(0xFFFFFFFFu, mb);
+    n = __reduce_add_sync(0xFFFFFFFFu, n);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sabs += __shfl_xor_sync(0xFFFFFFFFu, sabs, o);
+    if ((tid & 31) == 0) {
+        stat[tid >> 5][0] = mb;
+        stat[tid >> 5][1] = n;
+        stat[tid >> 5][2] = __float_as_uint(sabs);
+    }
+    __syncthreads();
+    mb = n = 0;
+    sabs = 0.f;
+#pragma unroll
+    for (int w = 0; w < kPrepThreads / 32; ++w) {
+        mb = max(mb, stat[w][0]);
+        n += stat[w][1];
+        sabs += __uint_as_float(stat[w][2]);
+    }
     if (tid == 0) {
         uint32_t *meta = it.meta + (size_t)kMetaWords * c;
         meta[2 * mm] = ma;
@@ -333,6 +325,28 @@ __global__ void __launch_bounds__(kPrepThreads) k_tern_bprep(const __grid_consta
             d[1] = rows[1];
         }
     }
+}
+
+// The MMAs of one stage's column `quad` for a chunk with two bands (4m B
+// rows per 16-code block, both B buffers from the first): N = 16 for m <= 4,
+// with four 128-code columns; N = 32 for m >= 5, with two 256-code columns
+// issued by quads 0 and 1 (quads 2 and 3 issue nothing).  Kept out of line:
+// it runs only for activations with outlier channels.
+__device__ __noinline__ void issue_two_band(uint32_t tmem, uint32_t bbuf, int g, int quad, int buf, int st, int m)
+{
+    const int n = mma_n(m, 2);
+    const int cols = n == 32 ? 2 : kCols;
+    if (quad >= cols) return;
+    const int steps = 16 / cols;  // K = 32 steps per column
+    const uint32_t wbytes = b_block_bytes(m, 2);
+    const uint32_t idesc = idesc_n(n);
+    const uint32_t d = tmem + kDCol + (uint32_t)(n * (cols * buf + quad));
+    const uint32_t a = tmem + (uint32_t)(g * 128 + quad * 8 * steps);
+    const uint64_t bd = b_desc_lbo(bbuf + (uint32_t)(st * kStageWords + 2 * steps * quad) * wbytes, wbytes);
+    const uint32_t bd_lo = (uint32_t)bd, bd_hi = (uint32_t)(bd >> 32), t_step = (2u * wbytes) >> 4;
+    for (int t = 0; t < steps; ++t)
+        ptx::mma_ts_f8f6f4_lh(d, a + 8u * (uint32_t)t, bd_lo + t_step * (uint32_t)t, bd_hi, idesc,
+                              (st != 0 || t != 0) ? 1u : 0u);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -453,6 +467,8 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
         int a_q = 0;               //          TMEM slot g, use s / kASlots
         uint32_t tpar = g == 0 ? 1u : 0u;  // stage 0 needs no turn
         int gs = 0, gc = 0;
+        uint32_t bw = 0;  // band word of chunk bw_gc
+        int bw_gc = -1;
         bool more = any;
         while (more) {
             const int n_st = cur.n_stages_chunk;
@@ -463,41 +479,6 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
             // barrier counts as complete.
             const uint32_t dempty = bars + kBarDEmpty + 8u * (uint32_t)buf;
             const uint32_t dpar = ((uint32_t)(gc >> 1) & 1u) ^ 1u;
-            // The chunk's band count, written by the staging warps before its
-            // BFull arrival, is read after this issuer's first turn wait in
-            // the chunk (the turn chain starts at the stage-0 issuer, which
-            // waited for BFull); then its MMA shape and descriptors hold for
-            // the rest of the chunk.
-            const volatile uint32_t *bands_word = words + 8 + kXmWords * buf + 16;
-            const uint32_t tag = (uint32_t)gc & 0x3FFFFFFFu;
-            uint32_t bw = ~0u;  // this issuer's copy of the band word (no chunk's tag yet)
-            int cols = 0, steps = 0;
-            uint32_t idesc = 0, d = 0, a = 0, bd_lo0 = 0, bd_hi = 0, t_step = 0, st_step = 0, shape_of = ~0u;
-            // MMA shape and B descriptors of the chunk for band word bw:
-            // four 128-code columns at N = 16; two 256-code columns, issued
-            // by warps 0 and 1, at N = 32 (warps 2 and 3 then keep the turn
-            // and barrier protocol but issue nothing)
-            auto set_shape = [&](uint32_t bw) {
-                if (bw == shape_of) return;
-                shape_of = bw;
-                const int bands = (int)(bw & 3u) == 2 ? 2 : 1;
-                const int n = mma_n(m, bands);
-                const uint32_t wbytes = b_block_bytes(m, bands);
-                cols = n == 32 ? 2 : kCols;
-                steps = 16 / cols;  // K = 32 steps per column
-                idesc = idesc_n(n);
-                d = tmem + kDCol + (uint32_t)(n * (cols * buf + quad));
-                a = tmem + (uint32_t)(g * 128 + quad * 8 * steps);  // 8 columns per step
-                // compact B: column q of stage st starts at word st*32 + 2*steps*q, its
-                // K=32 step t at A column +8t and B word +2t; a two-band chunk fills
-                // both B buffers from the first
-                const uint32_t bsrc = bbuf + (bands == 2 ? 0u : (uint32_t)buf * kBBufBytes);
-                const uint64_t bd = b_desc_lbo(bsrc + (uint32_t)(2 * steps * quad) * wbytes, wbytes);
-                bd_lo0 = (uint32_t)bd;
-                bd_hi = (uint32_t)(bd >> 32);
-                t_step = (2u * wbytes) >> 4;
-                st_step = ((uint32_t)kStageWords * wbytes) >> 4;
-            };
             for (int st = (g - gs % kDecGroups + kDecGroups) % kDecGroups; st < n_st; st += kDecGroups) {
                 const uint32_t wf = bars + kBarWFull + 8 * w_r;
                 const uint32_t wpar = (uint32_t)w_q & 1u, apar = (uint32_t)a_q & 1u;
@@ -530,13 +511,6 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                 if (lane == 0) {
                     const uint32_t bpar = (uint32_t)(gc >> 1) & 1u;
                     const uint32_t bfull = bars + kBarBFull + 8 * buf;
-                    // The band word as it stands now, usually already this
-                    // chunk's (the staging warps run ahead): its MMA shape and
-                    // descriptors are then ready before the turn comes.
-                    if ((bw >> 2) != tag) {
-                        bw = *bands_word;
-                        set_shape(bw);
-                    }
                     // The turn first: once it has come, chunk gc - 2 (the same B
                     // buffer) has passed its own BFull wait and the epilogue
                     // before the one waited for here is done, so neither
@@ -548,23 +522,35 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                                               (ptx::mbar_try_wait(dempty, dpar) || waiter.wait(dempty, dpar))));
                     if (lok) {
                         ptx::tc_fence_after();
-                        // a word read before the waits may have been the previous
-                        // chunk's on this buffer: its tag tells, read it again
-                        if ((bw >> 2) != tag) {
-                            bw = *bands_word;
-                            set_shape(bw);
+                        // The chunk's band count, written by the staging warps
+                        // before their BFull arrival, read once per chunk: the
+                        // stage-0 issuer waited for BFull and every later
+                        // stage's issuer follows it through the turn chain,
+                        // while the word is rewritten only after this chunk's
+                        // last stage has been issued.
+                        if (bw_gc != gc) {
+                            bw = words[8 + kXmWords * buf + 16];
+                            bw_gc = gc;
                         }
-                        if (quad < cols) {
-                            const uint32_t bd_lo = bd_lo0 + st_step * (uint32_t)st;
-                            ptx::mma_ts_f8f6f4_lh(d, a, bd_lo, bd_hi, idesc, st != 0 ? 1u : 0u);
+                        if ((bw & 3u) != 2u) {
+                            // one band: N = 16 (2m <= 16); compact B, column q
+                            // of stage st at word st*32 + 8q, its K = 32 step t
+                            // at A column +8t and B word +2t
+                            const uint32_t wbytes = b_block_bytes(m, 1);
+                            const uint32_t d = tmem + kDCol + 16u * (uint32_t)(kCols * buf + quad);
+                            const uint32_t a = tmem + (uint32_t)(g * 128 + quad * 32);
+                            const uint64_t bd = b_desc_lbo(bbuf + (uint32_t)buf * kBBufBytes +
+                                                               (uint32_t)(st * kStageWords + 8 * quad) * wbytes,
+                                                           wbytes);
+                            const uint32_t bd_lo = (uint32_t)bd, bd_hi = (uint32_t)(bd >> 32);
+                            const uint32_t t_step = (2u * wbytes) >> 4;
+                            constexpr uint32_t kIdesc16 = idesc_n(16);
+                            ptx::mma_ts_f8f6f4_lh(d, a, bd_lo, bd_hi, kIdesc16, st != 0 ? 1u : 0u);
 #pragma unroll
                             for (int t = 1; t < 4; ++t)
-                                ptx::mma_ts_f8f6f4_lh(d, a + 8u * t, bd_lo + t_step * t, bd_hi, idesc, 1u);
-                            if (cols == 2) {
-#pragma unroll
-                                for (int t = 4; t < 8; ++t)
-                                    ptx::mma_ts_f8f6f4_lh(d, a + 8u * t, bd_lo + t_step * t, bd_hi, idesc, 1u);
-                            }
+                                ptx::mma_ts_f8f6f4_lh(d, a + 8u * t, bd_lo + t_step * t, bd_hi, kIdesc16, 1u);
+                        } else {
+                            issue_two_band(tmem, bbuf, g, quad, buf, st, m);
                         }
                         ptx::tc_fence_before();
                         ptx::mbar_arrive(next_turn);  // the next stage's MMAs on this column follow these
@@ -596,9 +582,13 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
         const int quad = warp & 3;
         const int i = quad * 32 + lane;               // tile row == TMEM lane
         ptx::grid_dep_wait();
-        // per activation row, the unit's sum so far as an unevaluated pair
-        // (see acc_pair): chunks and bands of one unit have their own scales
+        // Per activation row, the unit's sum so far.  While every chunk of the
+        // unit has had one band it is a plain fp32 sum: the band choice
+        // already keeps each chunk within 2^-24 of its sum|x|.  From the first
+        // two-band chunk on (outlier channels, whose partial sums may cancel
+        // far below their own size) it is an unevaluated pair (acc_pair).
         float acc[8], acc_lo[8];
+        bool pairs = false;
 #pragma unroll
         for (int n = 0; n < 8; ++n) acc[n] = acc_lo[n] = 0.f;
         // previous chunk, whose accumulators are read after the next chunk's B is staged
@@ -622,58 +612,62 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
             const uint32_t *xm = meta_s + kXmWords * eb;
             const int bands = (int)(xm[16] & 3u);
             const int n = mma_n(it.m, bands), cols = n == 32 ? 2 : kCols;
+            pairs = pairs || bands == 2;
             uint32_t good = 1u;
             if (lane == 0) good = waiter.wait(bars + kBarDFull + 8 * eb, (e >> 1) & 1) ? 1u : 0u;
             good = __shfl_sync(0xFFFFFFFFu, good, 0);
+            // one band: column 2i holds the hi, 2i + 1 the lo terms of row i,
+            // summed over the issuing columns here and scaled once D is free
+            float dsum[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) dsum[q] = 0.f;
             if (good) {
                 ptx::tc_fence_after();
                 const uint32_t base = tmem + ((uint32_t)(quad * 32) << 16) + kDCol + (uint32_t)(n * cols * eb);
-                if (it.m == 1 && bands == 1) {  // the decode-time GEMV: two live columns
-                    float d0 = 0.f, d1 = 0.f;
-#pragma unroll 1
-                    for (int c = 0; c < cols; ++c) {
-                        uint32_t dv[4];
-                        ptx::tmem_ld_32x32b_x4(base + (uint32_t)(n * c), dv);
-                        ptx::tmem_wait_ld();
-                        d0 += __uint_as_float(dv[0]);
-                        d1 += __uint_as_float(dv[1]);
+                if (bands == 1 && it.m == 1) {  // the decode-time GEMV: two live columns of each
+                    uint32_t dv[kCols][4];
+#pragma unroll
+                    for (int c = 0; c < kCols; ++c) ptx::tmem_ld_32x32b_x4(base + 16u * (uint32_t)c, dv[c]);
+                    ptx::tmem_wait_ld();
+#pragma unroll
+                    for (int c = 0; c < kCols; ++c) {
+                        dsum[0] += __uint_as_float(dv[c][0]);
+                        dsum[1] += __uint_as_float(dv[c][1]);
                     }
-                    const int sa = row_scale_exp(xm[0]);
-                    acc_pair(acc[0], acc_lo[0], fmaf(d1, exp2i(-sa - 4), d0 * exp2i(-sa)));
-                } else
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {  // TMEM columns 16h .. 16h+15 of every issuing column
-                    if (16 * h >= 2 * bands * it.m) break;
-                    float dsum[16];
-#pragma unroll
-                    for (int q = 0; q < 16; ++q) dsum[q] = 0.f;
+                } else if (bands == 1) {
 #pragma unroll 1
-                    for (int c = 0; c < cols; ++c) {
+                    for (int c = 0; c < kCols; ++c) {
                         uint32_t dv[16];
-                        ptx::tmem_ld_32x32b_x16(base + (uint32_t)(n * c + 16 * h), dv);
+                        ptx::tmem_ld_32x32b_x16(base + 16u * (uint32_t)c, dv);
                         ptx::tmem_wait_ld();
 #pragma unroll
                         for (int q = 0; q < 16; ++q) dsum[q] += __uint_as_float(dv[q]);
                     }
-                    if (bands == 1) {  // column 2i: hi, 2i + 1: lo of row i (h == 0)
+                } else {
+                    // two bands: column 4i + b holds hi_A, lo_A, hi_B, lo_B of
+                    // row i, rows 4h .. 4h + 3 in TMEM columns 16h .. 16h + 15
+                    // of every issuing column; each band's total goes into
+                    // the row's pair
+                    for (int h = 0; h < 2 && 16 * h < 4 * it.m; ++h) {
+                        float d2[16];
 #pragma unroll
-                        for (int mm = 0; mm < 8; ++mm) {
-                            if (h == 0 && mm < it.m) {
-                                const int sa = row_scale_exp(xm[2 * mm]);
-                                acc_pair(acc[mm], acc_lo[mm],
-                                         fmaf(dsum[2 * mm + 1], exp2i(-sa - 4), dsum[2 * mm] * exp2i(-sa)));
-                            }
+                        for (int q = 0; q < 16; ++q) d2[q] = 0.f;
+                        for (int c = 0; c < cols; ++c) {
+                            uint32_t dv[16];
+                            ptx::tmem_ld_32x32b_x16(base + (uint32_t)(n * c + 16 * h), dv);
+                            ptx::tmem_wait_ld();
+#pragma unroll
+                            for (int q = 0; q < 16; ++q) d2[q] += __uint_as_float(dv[q]);
                         }
-                    } else {  // column 4i + b: hi_A, lo_A, hi_B, lo_B of row i
 #pragma unroll
                         for (int r = 0; r < 4; ++r) {
                             const int mm = 4 * h + r;
                             if (mm < it.m) {
                                 const int sa = row_scale_exp(xm[2 * mm]), sb = row_scale_exp(xm[2 * mm + 1]);
                                 acc_pair(acc[mm], acc_lo[mm],
-                                         fmaf(dsum[4 * r + 1], exp2i(-sa - 4), dsum[4 * r] * exp2i(-sa)));
+                                         fmaf(d2[4 * r + 1], exp2i(-sa - 4), d2[4 * r] * exp2i(-sa)));
                                 acc_pair(acc[mm], acc_lo[mm],
-                                         fmaf(dsum[4 * r + 3], exp2i(-sb - 4), dsum[4 * r + 2] * exp2i(-sb)));
+                                         fmaf(d2[4 * r + 3], exp2i(-sb - 4), d2[4 * r + 2] * exp2i(-sb)));
                             }
                         }
                     }
@@ -682,9 +676,23 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(bars + kBarDEmpty + 8 * eb);
+            if (good && bands == 1) {
+#pragma unroll
+                for (int mm = 0; mm < 8; ++mm) {
+                    if (mm < it.m) {
+                        const int sa = row_scale_exp(xm[2 * mm]);
+                        const float t = fmaf(dsum[2 * mm + 1], exp2i(-sa - 4), dsum[2 * mm] * exp2i(-sa));
+                        if (pairs)
+                            acc_pair(acc[mm], acc_lo[mm], t);
+                        else
+                            acc[mm] += t;
+                    }
+                }
+            }
             if (!prev_last) return;
 #pragma unroll
             for (int q = 0; q < 8; ++q) acc[q] = __fadd_rn(acc[q], acc_lo[q]);
+            pairs = false;
             if (it.swiglu) {
                 const int r = prev_tile * 64 + (i & 63);
                 if (i >= 64 && r < it.rows) {
@@ -771,9 +779,9 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                     // on BFull (whose phase also waits for every staging
                     // thread's arrival below), with two a build from x here
                     const uint32_t *meta = it.meta + (size_t)kMetaWords * cur.chunk;
-                    uint32_t two = 0;
-                    for (int q = 0; q < m; ++q) two |= meta[16 + q];
-                    bands = two != 0u ? 2 : 1;
+                    // each warp reads the rows' flags side by side (one load latency)
+                    const uint32_t flag = lane < m ? meta[16 + lane] : 0u;
+                    bands = __any_sync(0xFFFFFFFFu, flag != 0u) ? 2 : 1;
                     if (st_tid < 2 * m) xm[st_tid] = meta[st_tid];
                     if (bands == 1) {
                         if (st_tid == 0) {
