@@ -59,7 +59,10 @@ def _load():
             lib.orc_silu.restype = ctypes.c_double
             lib.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
             lib.orc_bf16_to_double.restype = ctypes.c_double
-            for f in (lib.orc_pack, lib.orc_unpack, lib.orc_stats, lib.orc_gemm, lib.orc_swiglu):
+            lib.orc_rmsnorm.argtypes = [p, p, i64, i64, ctypes.c_double, p, p]
+            lib.orc_rmsnorm_gemm.argtypes = [p, p, i64, i64, p, p, ctypes.c_double, i64, p, p, i64, i64]
+            for f in (lib.orc_pack, lib.orc_unpack, lib.orc_stats, lib.orc_gemm, lib.orc_swiglu, lib.orc_rmsnorm,
+                      lib.orc_rmsnorm_gemm):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -181,3 +184,48 @@ def silu(z: float) -> float:
 
 def bf16_to_double(bits: int) -> float:
     return _load().orc_bf16_to_double(int(bits))
+
+
+def rmsnorm(x_bits: np.ndarray, g: np.ndarray, eps: float = 1e-6):
+    """RMSNorm of each activation row, rounded to bf16 (see orc_rmsnorm).
+
+    Returns (xn_bits uint16 [m, k], r float32 [m]) where r is each row's
+    fp32 factor 1 / sqrt(mean x^2 + eps)."""
+    x_bits = np.ascontiguousarray(np.atleast_2d(x_bits), dtype=np.uint16)
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    m, k = x_bits.shape
+    assert g.shape == (k,)
+    xn = np.zeros((m, k), dtype=np.uint16)
+    r = np.zeros(m, dtype=np.float32)
+    _check(_load().orc_rmsnorm(_ptr(x_bits), _ptr(g), m, k, float(eps), _ptr(xn), _ptr(r)), "rmsnorm")
+    return xn, r
+
+
+def rmsnorm_gemm(codes, scale, k: int, x_bits: np.ndarray, g: np.ndarray, eps: float = 1e-6,
+                 threads: int = 1, rows_subset=None) -> np.ndarray:
+    """y [m, rows] float64 = scale * (T @ rmsnorm(x)): the projection that
+    follows a norm (q/k/v after the attention norm)."""
+    xn, _ = rmsnorm(x_bits, g, eps)
+    return gemm(codes, scale, k, xn, threads=threads, rows_subset=rows_subset)
+
+
+def rmsnorm_gemm_c(codes, scale, k: int, x_bits: np.ndarray, g: np.ndarray, eps: float = 1e-6) -> np.ndarray:
+    """rmsnorm_gemm through the C composite orc_rmsnorm_gemm (one thread)."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint32)
+    scale = np.ascontiguousarray(scale, dtype=np.float32)
+    x_bits = np.ascontiguousarray(np.atleast_2d(x_bits), dtype=np.uint16)
+    g = np.ascontiguousarray(g, dtype=np.float32)
+    rows = codes.shape[0]
+    m = x_bits.shape[0]
+    xn = np.zeros((m, k), dtype=np.uint16)
+    y = np.zeros((m, rows), dtype=np.float64)
+    _check(_load().orc_rmsnorm_gemm(_ptr(codes), _ptr(scale), rows, k, _ptr(x_bits), _ptr(g), float(eps), m,
+                                    _ptr(xn), _ptr(y), 0, rows), "rmsnorm_gemm")
+    return y
+
+
+def rmsnorm_swiglu(g_codes, g_scale, u_codes, u_scale, k: int, x_bits: np.ndarray, g: np.ndarray,
+                   eps: float = 1e-6, threads: int = 1, rows_subset=None) -> np.ndarray:
+    """h = silu(gate) * up on rmsnorm(x): the feed-forward block's first step."""
+    xn, _ = rmsnorm(x_bits, g, eps)
+    return swiglu(g_codes, g_scale, u_codes, u_scale, k, xn, threads=threads, rows_subset=rows_subset)

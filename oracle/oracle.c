@@ -180,3 +180,66 @@ int orc_swiglu(const uint32_t *gate_codes, const float *gate_scale,
     }
     return ORC_OK;
 }
+
+/*
+ * RMSNorm ahead of a projection (Neutrino-1 8B model page, spec table:
+ * RMSNorm with eps 1e-6 before the attention and feed-forward blocks, whose
+ * first linears are q/k/v and gate/up).  For each activation row i the page
+ * gives only the textbook operation
+ *
+ *     xn[i][k] = g[k] * x[i][k] / sqrt(mean_k x[i][k]^2 + eps)
+ *
+ * with a learned per-channel weight g (fp32 here).  The projection consumes
+ * bf16 activations, so xn is rounded to bf16 once, and this project fixes
+ * the precision of every step, because that rounding is a quantisation the
+ * CUDA path must reach bit for bit:
+ *   - the mean square in double, summing x^2 in increasing k (each bf16
+ *     square is exact in double), divided by K;
+ *   - the row factor r = 1 / sqrt(mean + eps) in double, rounded to fp32;
+ *   - per element, fp32 products in this order: v = x * r, then g * v;
+ *   - v rounded to bf16, round to nearest even (finite inputs).
+ */
+static uint16_t orc_float_to_bf16_rne(float f)
+{
+    union { float f; uint32_t u; } v;
+    v.f = f;
+    const uint32_t lsb = (v.u >> 16) & 1u;
+    return (uint16_t)((v.u + 0x7FFFu + lsb) >> 16);
+}
+
+int orc_rmsnorm(const uint16_t *x, const float *g, int64_t m, int64_t k, double eps,
+                uint16_t *xn, float *r_out)
+{
+    if (m < 0 || k <= 0 || eps < 0.0) return ORC_BAD_SHAPE;
+    for (int64_t mi = 0; mi < m; ++mi) {
+        const uint16_t *xr = x + mi * k;
+        double ss = 0.0;
+        for (int64_t c = 0; c < k; ++c) {
+            const double v = orc_bf16_to_double(xr[c]);
+            ss += v * v;
+        }
+        const float r = (float)(1.0 / sqrt(ss / (double)k + eps));
+        if (r_out) r_out[mi] = r;
+        for (int64_t c = 0; c < k; ++c) {
+            volatile float xv = (float)orc_bf16_to_double(xr[c]);
+            volatile float v = xv * r;   /* fp32 product, rounded */
+            volatile float w = g[c] * v; /* fp32 product, rounded */
+            xn[mi * k + c] = orc_float_to_bf16_rne(w);
+        }
+    }
+    return ORC_OK;
+}
+
+/*
+ * The normalised projection: y = scale * (T @ rmsnorm(x)), i.e. orc_rmsnorm
+ * followed by orc_gemm on its bf16 output, for rows [row_begin, row_end).
+ * xn_scratch: m * k uint16 of caller memory.
+ */
+int orc_rmsnorm_gemm(const uint32_t *codes, const float *scale, int64_t rows, int64_t k,
+                     const uint16_t *x, const float *g, double eps, int64_t m,
+                     uint16_t *xn_scratch, double *y, int64_t row_begin, int64_t row_end)
+{
+    const int rc = orc_rmsnorm(x, g, m, k, eps, xn_scratch, (float *)0);
+    if (rc != ORC_OK) return rc;
+    return orc_gemm(codes, scale, rows, k, xn_scratch, m, y, row_begin, row_end);
+}
