@@ -100,7 +100,8 @@ typedef enum {
     TERN_ERR_M_RANGE = 6, /* m outside [1, TERN_MAX_M] */
     TERN_ERR_CUDA = 7,    /* a CUDA runtime call or launch failed */
     TERN_ERR_TIMEOUT = 8, /* a device-side bounded wait ran out (see tern_last_device_error) */
-    TERN_ERR_VALUE = 9    /* an int8 weight given to tern_pack is not -1, 0 or +1 */
+    TERN_ERR_VALUE = 9    /* a value outside its range: an int8 weight given to tern_pack that is
+                             not -1, 0 or +1, or an RMSNorm eps that is negative or not finite */
 } tern_status;
 
 /* One packed ternary matrix.  Pointers are device pointers for the device
@@ -215,6 +216,27 @@ TERN_API tern_status tern_gemm_batched(const tern_batch_item *items, int32_t n, 
  * (-TERN_ERR_NULL).  Not an operation of the model pages: a planning aid for
  * callers that count or capture launches. */
 TERN_API int32_t tern_gemm_batched_launches(const tern_batch_item *items, int32_t n);
+
+/* tern_gemm_batched with an RMSNorm ahead of each item's projection (model
+ * page spec table: RMSNorm with eps 1e-6 before the attention and
+ * feed-forward blocks, whose first linears are q/k/v and gate/up).  For an
+ * item i with norm_w[i] != NULL, each activation row x[j] is first replaced
+ * by xn[j][c] = bf16_rn(norm_w[i][c] * fl32(x[j][c] * r_j)), with
+ * r_j = fl32(1 / sqrt(mean_c x[j][c]^2 + eps)) (mean over the item's k
+ * channels, taken in fp64; eps widened to fp64): the page gives only the
+ * textbook operation, and this library rounds the normalised activations to
+ * bf16 because the projection consumes bf16.  Items with norm_w[i] == NULL
+ * run as in tern_gemm_batched.  x itself is not modified.
+ * norm_w: host array of n pointers; each non-NULL entry is a device array of
+ * the item's k fp32 channel weights, 16-byte aligned.  eps: finite, >= 0.
+ * Launches, workspace and checks are those of tern_gemm_batched, plus
+ * TERN_ERR_NULL (norm_w == NULL with n > 0), TERN_ERR_VALUE (eps negative,
+ * NaN or infinite) and TERN_ERR_ALIGN (a misaligned norm_w[i]).
+ * Accuracy: r_j is rounded from an fp64 sum whose order is the kernel's own,
+ * so in rare rows it may differ from a sequential sum's by one fp32 ulp;
+ * everything else is fixed above. */
+TERN_API tern_status tern_gemm_batched_rmsnorm(const tern_batch_item *items, const float *const *norm_w,
+                                               float eps, int32_t n, void *stream);
 
 /* tern_gemm_batched for callers that must not allocate device memory: code
  * running inside a memory budget that another allocator owns (a serving

@@ -38,7 +38,7 @@ TERN_NOALLOC_WS_BYTES = 4194304
 ABI_FUNCTIONS = (
     "tern_pack", "tern_validate", "tern_unpack", "tern_gemv", "tern_gemv_swiglu",
     "tern_gemm_smallm", "tern_gemm_smallm_swiglu", "tern_gemm_batched", "tern_gemm_batched_launches",
-    "tern_gemm_batched_noalloc",
+    "tern_gemm_batched_noalloc", "tern_gemm_batched_rmsnorm",
     "tern_last_device_error", "tern_set_wait_limit",
     "tern_status_str", "tern_abi_version",
 )
@@ -87,6 +87,7 @@ def load(path: str | None = None):
             "tern_gemm_batched": [vp, i32, vp],
             "tern_gemm_batched_launches": [vp, i32],
             "tern_gemm_batched_noalloc": [vp, i32, vp],
+            "tern_gemm_batched_rmsnorm": [vp, vp, ctypes.c_float, i32, vp],
             "tern_last_device_error": [vp],
             "tern_set_wait_limit": [ctypes.c_int64],
             "tern_status_str": [ctypes.c_int],
@@ -238,6 +239,21 @@ def tern_gemm_batched_noalloc(items, stream=None):
     arr = items if isinstance(items, ctypes.Array) else batch_items(items)
     _check(load().tern_gemm_batched_noalloc(ctypes.cast(arr, ctypes.c_void_p) if len(arr) else None, len(arr),
                                             _stream_handle(stream)), "tern_gemm_batched_noalloc")
+
+
+def tern_gemm_batched_rmsnorm(items, norm_w, eps: float = 1e-6, stream=None):
+    """tern_gemm_batched with an RMSNorm ahead of each item whose entry in
+    norm_w (a sequence of device fp32 [k] tensors or None, one per item) is
+    not None."""
+    arr = items if isinstance(items, ctypes.Array) else batch_items(items)
+    if len(norm_w) != len(arr):
+        raise ValueError("norm_w needs one entry per item")
+    ptrs = (ctypes.c_void_p * max(1, len(arr)))()
+    for i, g in enumerate(norm_w):
+        ptrs[i] = None if g is None else _dptr(g)
+    _check(load().tern_gemm_batched_rmsnorm(ctypes.cast(arr, ctypes.c_void_p) if len(arr) else None,
+                                            ctypes.cast(ptrs, ctypes.c_void_p), ctypes.c_float(eps), len(arr),
+                                            _stream_handle(stream)), "tern_gemm_batched_rmsnorm")
 
 
 def tern_gemm_batched_launches(items) -> int:

@@ -111,10 +111,12 @@ struct Item {
     // holds its rows' maxima and band-B flags.
     const unsigned char *bsrc;
     const uint32_t *meta;
+    const float *norm_w;  // RMSNorm channel weights [k], or nullptr: x enters as given
 };
 
 struct Params {
     int n_items;
+    float eps;                     // RMSNorm eps of the items with norm weights
     long long wait_limit;          // bound of every Waiter, in cycles
     int unit_start[kMaxCtas + 1];  // CTA b runs units [unit_start[b], unit_start[b + 1])
     int item_start[kMaxCtas];      // the item holding unit unit_start[b]
@@ -141,12 +143,13 @@ constexpr uint32_t kBarDEmpty = kBarDFull + 16;
 constexpr uint32_t kBarDrain = kBarDEmpty + 16;  // one commit per issuing warp on exit
 constexpr uint32_t kBarTurn = kBarDrain + 8;     // [kCols][kDecGroups]: group g's turn on column q
 constexpr uint32_t kWordsOff = kBarTurn + 8 * kCols * kDecGroups;
-// words: [0] tmem base, [1] abort, [8..31] B buffer 0's chunk metadata,
-// [32..55] buffer 1's: per activation row i, [2i] row maximum and [2i + 1]
+// words: [0] tmem base, [1] abort, [8..39] B buffer 0's chunk metadata,
+// [40..71] buffer 1's: per activation row i, [2i] row maximum and [2i + 1]
 // band-B maximum; [16] the chunk's number times 4 plus its band count; [17],
-// [18] scratch of the m = 1 build
-constexpr uint32_t kWordsCount = 64;
-constexpr uint32_t kXmWords = 24;
+// [18] scratch of the m = 1 build; [24 + i] row i's RMSNorm factor (fp32
+// bits; items with a norm)
+constexpr uint32_t kWordsCount = 72;
+constexpr uint32_t kXmWords = 32;
 constexpr uint32_t kSmemBytes = 1024 + kOffBar + kWordsOff + kWordsCount * 4;
 
 __device__ unsigned int g_batched_error;
@@ -216,11 +219,12 @@ constexpr int kPrepWords = 7;           // words per thread: 28 stages * 32 / 12
 constexpr uint32_t kBulkPiece = 16384;  // bytes per bulk copy of a prepared chunk
 // Per-chunk metadata (32 words): for activation row i, [2i] its maximum and
 // [2i + 1] its band-B maximum (fp32 bits of |x|), [16 + i] 1 if it needs
-// band B.
+// band B, [24 + i] its RMSNorm factor (items with a norm).
 constexpr int kMetaWords = 32;
 
 struct PrepItem {
     const uint16_t *x;
+    const float *norm_w;  // RMSNorm channel weights [k], or nullptr
     unsigned char *b;
     uint32_t *meta;
     int k, m, stages, cstages;
@@ -229,6 +233,7 @@ struct PrepItem {
 
 struct PrepParams {
     int n_items, n_tasks;
+    float eps;
     PrepItem item[kMaxItems];
 };
 
@@ -248,6 +253,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_tern_bprep(const __grid_consta
 {
     __shared__ uint32_t red[kPrepThreads / 32];
     __shared__ uint32_t stat[kPrepThreads / 32][3];
+    __shared__ double ssred[kPrepThreads / 32];
     // The persistent kernel that follows may start at once: its weight stream
     // needs nothing from here, and its staging warps wait for this grid to
     // finish before they read the workspace.  The previous kernel on the
@@ -272,6 +278,27 @@ __global__ void __launch_bounds__(kPrepThreads) k_tern_bprep(const __grid_consta
         if (wi < nw && gw < kw) {
             va[q] = __ldg(xr + 2 * gw);
             vb[q] = __ldg(xr + 2 * gw + 1);
+        }
+    }
+    float rn = 0.f;
+    if (it.norm_w != nullptr) {
+        // RMSNorm: the mean square over the whole row (every chunk's CTA of
+        // the row takes it), then this chunk's words normalised in place
+        double ss = 0.0;
+        for (int w = tid; w < kw; w += kPrepThreads) ss += sumsq16(__ldg(xr + 2 * w), __ldg(xr + 2 * w + 1));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+        if ((tid & 31) == 0) ssred[tid >> 5] = ss;
+        __syncthreads();
+        ss = 0.0;
+#pragma unroll
+        for (int w = 0; w < kPrepThreads / 32; ++w) ss += ssred[w];
+        rn = rms_factor(ss, it.k, p.eps);
+        const float4 *g4 = reinterpret_cast<const float4 *>(it.norm_w);
+#pragma unroll
+        for (int q = 0; q < kPrepWords; ++q) {
+            const int wi = tid + q * kPrepThreads, gw = w0 + wi;
+            if (wi < nw && gw < kw) rmsnorm_word(va[q], vb[q], g4 + 4 * gw, rn);
         }
     }
     uint32_t mx = 0;
@@ -310,6 +337,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_tern_bprep(const __grid_consta
         meta[2 * mm] = ma;
         meta[2 * mm + 1] = mb;
         meta[16 + mm] = need_two_bands(ma, n, sabs) ? 1u : 0u;
+        meta[24 + mm] = __float_as_uint(rn);
     }
     const float sc = exp2i(row_scale_exp(ma));
     const size_t wbytes = b_block_bytes(it.m, 1);
@@ -729,7 +757,8 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                 waiter.wait(bars + kBarBEmpty + 8 * ((gc - 1) & 1), (uint32_t)((gc - 1) >> 1) & 1u);
             __syncwarp();
         };
-        // Two-band operand of a chunk from x in global memory, with each
+        // Two-band operand of a chunk from x in global memory (normalised
+        // again with the row's factor for items with a norm), with each
         // row's maxima already in xm (both buffers, from the first; the
         // callers have waited for them).
         auto build_two_band = [&](const Item &it, int w0, int n_words, const uint32_t *xm) {
@@ -743,6 +772,9 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                     const uint4 *xr = reinterpret_cast<const uint4 *>(it.x + (size_t)mm * it.k) + 2 * gw;
                     va = xr[0];
                     vb = xr[1];
+                    if (it.norm_w != nullptr)
+                        rmsnorm_word(va, vb, reinterpret_cast<const float4 *>(it.norm_w) + 4 * gw,
+                                     __uint_as_float(xm[24 + mm]));
                 }
                 uint4 rows[4];
                 split_word2(va, vb, exp2i(row_scale_exp(xm[2 * mm])), exp2i(row_scale_exp(xm[2 * mm + 1])),
@@ -783,6 +815,7 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                     const uint32_t flag = lane < m ? meta[16 + lane] : 0u;
                     bands = __any_sync(0xFFFFFFFFu, flag != 0u) ? 2 : 1;
                     if (st_tid < 2 * m) xm[st_tid] = meta[st_tid];
+                    if (it.norm_w != nullptr && st_tid < m) xm[24 + st_tid] = meta[24 + st_tid];
                     if (bands == 1) {
                         if (st_tid == 0) {
                             const uint32_t bytes = (uint32_t)n_words * b_block_bytes(m, 1);
@@ -820,6 +853,31 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                         const uint16_t *src = in_k ? it.x + kk : it.x;
                         ptx::cp_async16(bb + 32u * (uint32_t)wi, src, in_k ? 16u : 0u);
                         ptx::cp_async16(bb + 32u * (uint32_t)wi + 16u, src + 8, in_k ? 16u : 0u);
+                    }
+                    if (it.norm_w != nullptr) {
+                        // RMSNorm: the row's mean square from x in global
+                        // memory over the whole row (while the copies fly),
+                        // then every thread's own words normalised in place
+                        const uint4 *xr = reinterpret_cast<const uint4 *>(it.x);
+                        const int kw = it.k / 16;
+                        double ss = 0.0;
+                        for (int w = st_tid; w < kw; w += kStagers) ss += sumsq16(__ldg(xr + 2 * w), __ldg(xr + 2 * w + 1));
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+                        double *ssred = reinterpret_cast<double *>(xch);  // free until this chunk's epilogue
+                        if (lane == 0) ssred[quad] = ss;
+                        ptx::named_bar_sync(1, kStagers);
+                        const float rn = rms_factor(ssred[0] + ssred[1] + ssred[2] + ssred[3], it.k, p.eps);
+                        if (st_tid == 0) xm[24] = __float_as_uint(rn);
+                        ptx::cp_async_wait_all();
+                        const float4 *g4 = reinterpret_cast<const float4 *>(it.norm_w);
+                        for (int wi = st_tid; wi < n_words && w0 + wi < kw; wi += kStagers) {
+                            const uint32_t at = bb + 32u * (uint32_t)wi;
+                            uint4 va = ptx::lds128(at), vb = ptx::lds128(at + 16u);
+                            rmsnorm_word(va, vb, g4 + 4 * (w0 + wi), rn);
+                            ptx::sts128(at, va);
+                            ptx::sts128(at + 16u, vb);
+                        }
                     }
                     ptx::cp_async_wait_all();
                     ptx::named_bar_sync(1, kStagers);
@@ -1024,7 +1082,10 @@ namespace {
 
 // Launches the batch.  fixed_ws: a workspace the caller guarantees to be
 // large enough for every launch group (nullptr: the per-stream workspace).
-tern_status run_batched(const tern_batch_item *items, int n, cudaStream_t stream, unsigned char *fixed_ws)
+// norm_w: nullptr, or per item the RMSNorm channel weights (nullptr for an
+// item without a norm), with eps.
+tern_status run_batched(const tern_batch_item *items, int n, cudaStream_t stream, unsigned char *fixed_ws,
+                        const float *const *norm_w = nullptr, float eps = 0.f)
 {
     static_assert(sizeof(Params) + sizeof(Maps) < 32000, "kernel parameters exceed 32 KB");
     const int sms = sm_count();
@@ -1067,6 +1128,7 @@ tern_status run_batched(const tern_batch_item *items, int n, cudaStream_t stream
             it.k = b.w->k;
             it.m = b.m;
             it.swiglu = b.up != nullptr;
+            it.norm_w = norm_w != nullptr ? norm_w[idx] : nullptr;
             chunk_plan(it.k, it.m, it.stages, it.cstages);
             it.unit0 = units;
             it.map = n_maps;
@@ -1082,6 +1144,7 @@ tern_status run_batched(const tern_batch_item *items, int n, cudaStream_t stream
         begin = end;
         if (cnt == 0) continue;
         prm.n_items = cnt;
+        prm.eps = eps;
         prm.wait_limit = wait_limit();
 
         // Items with m >= 2 take their B from the workspace, written by one
@@ -1091,6 +1154,7 @@ tern_status run_batched(const tern_batch_item *items, int n, cudaStream_t stream
         // with m = 1 are built by the persistent kernel's staging warps.
         PrepParams pp;
         std::memset(&pp, 0, sizeof(pp));
+        pp.eps = eps;
         size_t ws_need = 0;
         std::vector<std::pair<size_t, size_t>> ws_off(cnt);
         for (int j = 0; j < cnt; ++j) {
@@ -1110,6 +1174,7 @@ tern_status run_batched(const tern_batch_item *items, int n, cudaStream_t stream
                 it.meta = reinterpret_cast<const uint32_t *>(ws + ws_off[j].second);
                 PrepItem &q = pp.item[pp.n_items++];
                 q.x = it.x;
+                q.norm_w = it.norm_w;
                 q.b = ws + ws_off[j].first;
                 q.meta = reinterpret_cast<uint32_t *>(ws + ws_off[j].second);
                 q.k = it.k;
@@ -1175,6 +1240,12 @@ tern_status run_batched(const tern_batch_item *items, int n, cudaStream_t stream
 tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t stream)
 {
     return run_batched(items, n, stream, nullptr);
+}
+
+tern_status gemm_batched_rmsnorm(const tern_batch_item *items, const float *const *norm_w, float eps, int n,
+                                 cudaStream_t stream)
+{
+    return run_batched(items, n, stream, nullptr, norm_w, eps);
 }
 
 tern_status gemm_batched_noalloc(const tern_batch_item *items, int n, cudaStream_t stream)

@@ -227,6 +227,18 @@ extern "C" tern_status tern_gemm_batched(const tern_batch_item *items, int32_t n
     return gemm_batched(items, n, (cudaStream_t)stream);
 }
 
+extern "C" tern_status tern_gemm_batched_rmsnorm(const tern_batch_item *items, const float *const *norm_w, float eps,
+                                                 int32_t n, void *stream)
+{
+    const tern_status st = check_batch(items, n);
+    if (st != TERN_OK || n == 0) return st;
+    if (norm_w == nullptr) return TERN_ERR_NULL;
+    if (!(eps >= 0.f && eps <= 3.4e38f)) return TERN_ERR_VALUE;  // also rejects NaN and +inf
+    for (int32_t i = 0; i < n; ++i)
+        if (norm_w[i] != nullptr && (reinterpret_cast<uintptr_t>(norm_w[i]) & 15u) != 0) return TERN_ERR_ALIGN;
+    return gemm_batched_rmsnorm(items, norm_w, eps, n, (cudaStream_t)stream);
+}
+
 extern "C" tern_status tern_gemm_batched_noalloc(const tern_batch_item *items, int32_t n, void *stream)
 {
     const tern_status st = check_batch(items, n);

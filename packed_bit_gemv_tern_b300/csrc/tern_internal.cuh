@@ -32,6 +32,9 @@ tern_status take_mma_error();
 // Number of kernel launches gemm_batched makes for these items (host only).
 int batched_launches(const tern_batch_item *items, int n);
 tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t s);
+// As gemm_batched, each item with norm_w[i] != nullptr normalised first (RMSNorm).
+tern_status gemm_batched_rmsnorm(const tern_batch_item *items, const float *const *norm_w, float eps, int n,
+                                 cudaStream_t s);
 // As gemm_batched, with the prepared activations in a fixed module-scope
 // scratch of TERN_NOALLOC_WS_BYTES (TERN_ERR_SHAPE, nothing launched, if a
 // launch group needs more).

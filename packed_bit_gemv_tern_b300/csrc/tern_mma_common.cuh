@@ -12,6 +12,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -245,6 +246,51 @@ __device__ __forceinline__ uint4 transpose_row(const uint32_t (&p)[8])
     const uint32_t p13 = p[1] | (p[3] << 16), p57 = p[5] | (p[7] << 16);
     return make_uint4(__byte_perm(p02, p46, 0x6420), __byte_perm(p02, p46, 0x7531), __byte_perm(p13, p57, 0x6420),
                       __byte_perm(p13, p57, 0x7531));
+}
+
+// RMSNorm prologue (model page spec table: RMSNorm, eps 1e-6, ahead of the
+// q/k/v and gate/up projections).  Per activation row the mean square is
+// taken in fp64 (every bf16 square is exact there), the row factor
+// r = 1 / sqrt(mean + eps) is rounded to fp32, and each element becomes
+// bf16_rn(g * fl32(x * r)): the projection then reads bf16 as without the
+// norm.  Only the order of the fp64 sum is the kernel's own.
+
+// Sum of the squares of the 16 bf16 activations of one word, in fp64.
+__device__ __forceinline__ double sumsq16(const uint4 a, const uint4 b)
+{
+    const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    double s = 0.0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const double lo = (double)__uint_as_float(v[j] << 16), hi = (double)__uint_as_float(v[j] & 0xFFFF0000u);
+        s = fma(lo, lo, s);
+        s = fma(hi, hi, s);
+    }
+    return s;
+}
+
+// Row factor from the row's fp64 sum of squares over k channels.
+__device__ __forceinline__ float rms_factor(double ss, int k, float eps)
+{
+    return (float)(1.0 / sqrt(ss / (double)k + (double)eps));
+}
+
+// One word of 16 bf16 activations, normalised in place: element j becomes
+// bf16_rn(g[j] * fl32(x[j] * r)); g4: its 16 channel weights.
+__device__ __forceinline__ void rmsnorm_word(uint4 &a, uint4 &b, const float4 *g4, float r)
+{
+    const float4 g0 = __ldg(g4), g1 = __ldg(g4 + 1), g2 = __ldg(g4 + 2), g3 = __ldg(g4 + 3);
+    const float g[16] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w, g2.x, g2.y, g2.z, g2.w, g3.x, g3.y, g3.z, g3.w};
+    uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float lo = __fmul_rn(g[2 * j], __fmul_rn(__uint_as_float(v[j] << 16), r));
+        const float hi = __fmul_rn(g[2 * j + 1], __fmul_rn(__uint_as_float(v[j] & 0xFFFF0000u), r));
+        v[j] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+               ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+    }
+    a = make_uint4(v[0], v[1], v[2], v[3]);
+    b = make_uint4(v[4], v[5], v[6], v[7]);
 }
 
 // One word (16 k) of one activation row -> its two one-band B rows: out[0]

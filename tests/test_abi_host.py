@@ -159,6 +159,22 @@ def test_device_entry_points_reject_before_launch(lib):
     assert lib.tern_gemm_batched(ctypes.cast(arr, ctypes.c_void_p), 2, None) == tern.TERN_ERR_SHAPE
     arr[1].up, arr[1].x = None, 0x3004
     assert lib.tern_gemm_batched(ctypes.cast(arr, ctypes.c_void_p), 2, None) == tern.TERN_ERR_ALIGN
+    # batched with an RMSNorm: the item checks first, then the norm arguments
+    arr[1].x = 0x3000
+    pa = ctypes.cast(arr, ctypes.c_void_p)
+    norms = (ctypes.c_void_p * 2)(0x6000, None)
+    pn = ctypes.cast(norms, ctypes.c_void_p)
+    f = lib.tern_gemm_batched_rmsnorm
+    assert f(None, None, ctypes.c_float(1e-6), 0, None) == tern.TERN_OK
+    assert f(None, pn, ctypes.c_float(1e-6), -1, None) == tern.TERN_ERR_SHAPE
+    assert f(pa, None, ctypes.c_float(1e-6), 2, None) == tern.TERN_ERR_NULL
+    for eps in (-1e-6, float("nan"), float("inf")):
+        assert f(pa, pn, ctypes.c_float(eps), 2, None) == tern.TERN_ERR_VALUE
+    norms[1] = 0x6004
+    assert f(pa, pn, ctypes.c_float(1e-6), 2, None) == tern.TERN_ERR_ALIGN
+    arr[1].m = 9  # a bad item is reported before the norm arguments
+    assert f(pa, None, ctypes.c_float(-1.0), 2, None) == tern.TERN_ERR_M_RANGE
+    arr[1].m = 1
     # empty problems succeed without a launch, with NULL pointers
     empty = tern.CMatrix(0, 64, None, None, None)
     assert lib.tern_gemv(ref(empty), None, None, None) == tern.TERN_OK
