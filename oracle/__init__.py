@@ -61,8 +61,10 @@ def _load():
             lib.orc_bf16_to_double.restype = ctypes.c_double
             lib.orc_rmsnorm.argtypes = [p, p, i64, i64, ctypes.c_double, p, p]
             lib.orc_rmsnorm_gemm.argtypes = [p, p, i64, i64, p, p, ctypes.c_double, i64, p, p, i64, i64]
+            lib.orc_i8_gemm.argtypes = [p, p, i64, i64, p, i64, p, p, i64, i64]
+            lib.orc_argmax.argtypes = [p, i64, i64, p]
             for f in (lib.orc_pack, lib.orc_unpack, lib.orc_stats, lib.orc_gemm, lib.orc_swiglu, lib.orc_rmsnorm,
-                      lib.orc_rmsnorm_gemm):
+                      lib.orc_rmsnorm_gemm, lib.orc_i8_gemm, lib.orc_argmax):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -229,3 +231,30 @@ def rmsnorm_swiglu(g_codes, g_scale, u_codes, u_scale, k: int, x_bits: np.ndarra
     """h = silu(gate) * up on rmsnorm(x): the feed-forward block's first step."""
     xn, _ = rmsnorm(x_bits, g, eps)
     return swiglu(g_codes, g_scale, u_codes, u_scale, k, xn, threads=threads, rows_subset=rows_subset)
+
+
+def i8_gemm(w: np.ndarray, scale: np.ndarray, x_bits: np.ndarray, threads: int = 1, rows_subset=None,
+            with_abs: bool = False):
+    """int8 head logits [m, rows] float64 = scale * (W @ x); with_abs also
+    returns scale * sum_k |w x| per logit (the fp32 error's yardstick)."""
+    w = np.ascontiguousarray(w, dtype=np.int8)
+    scale = np.ascontiguousarray(scale, dtype=np.float32)
+    x_bits = np.ascontiguousarray(np.atleast_2d(x_bits), dtype=np.uint16)
+    rows, k = w.shape
+    m = x_bits.shape[0]
+    assert x_bits.shape[1] == k
+    y = np.zeros((m, rows), dtype=np.float64)
+    a = np.zeros((m, rows), dtype=np.float64)
+    lib = _load()
+    _run_rows(lambda b, e: lib.orc_i8_gemm(_ptr(w), _ptr(scale), rows, k, _ptr(x_bits), m, _ptr(y), _ptr(a), b, e),
+              rows, threads, rows_subset)
+    return (y, a) if with_abs else y
+
+
+def argmax(y: np.ndarray) -> np.ndarray:
+    """Per row of y [m, rows]: the index of the largest value, lowest on ties."""
+    y = np.ascontiguousarray(np.atleast_2d(y), dtype=np.float64)
+    m, rows = y.shape
+    idx = np.zeros(m, dtype=np.int64)
+    _check(_load().orc_argmax(_ptr(y), m, rows, _ptr(idx)), "argmax")
+    return idx

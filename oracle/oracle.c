@@ -243,3 +243,52 @@ int orc_rmsnorm_gemm(const uint32_t *codes, const float *scale, int64_t rows, in
     if (rc != ORC_OK) return rc;
     return orc_gemm(codes, scale, rows, k, xn_scratch, m, y, row_begin, row_end);
 }
+
+/*
+ * int8 LM head (Neutrino-1 8B model page, "Where the bytes live": the output
+ * head is a 151,936 x 4,096 int8 matrix with per-row scales, read once per
+ * generated token; the speculative-decoding paragraph: the verifier accepts
+ * draft tokens greedily, i.e. by the argmax of each position's logits):
+ *
+ *     logit[m][r] = scale[r] * sum_k w[r][k] * x[m][k],   w int8, x bf16
+ *
+ * in double (every product is exact, the sum runs in increasing k), for rows
+ * [row_begin, row_end).  abs_out (may be NULL) receives
+ * scale[r] * sum_k |w[r][k] * x[m][k]|, the size an fp32 evaluation's
+ * rounding error is measured against.
+ */
+int orc_i8_gemm(const int8_t *w, const float *scale, int64_t rows, int64_t k,
+                const uint16_t *x, int64_t m, double *y, double *abs_out,
+                int64_t row_begin, int64_t row_end)
+{
+    if (rows < 0 || k < 0 || m < 0) return ORC_BAD_SHAPE;
+    for (int64_t mi = 0; mi < m; ++mi) {
+        for (int64_t r = row_begin; r < row_end; ++r) {
+            double acc = 0.0, aacc = 0.0;
+            for (int64_t c = 0; c < k; ++c) {
+                const double p = (double)w[r * k + c] * orc_bf16_to_double(x[mi * k + c]);
+                acc += p;
+                aacc += fabs(p);
+            }
+            y[mi * rows + r] = (double)scale[r] * acc;
+            if (abs_out) abs_out[mi * rows + r] = fabs((double)scale[r]) * aacc;
+        }
+    }
+    return ORC_OK;
+}
+
+/*
+ * Greedy choice per activation row: the index of the largest value of
+ * y[mi][0..rows), the lowest index among equal maxima.  rows > 0.
+ */
+int orc_argmax(const double *y, int64_t m, int64_t rows, int64_t *idx)
+{
+    if (m < 0 || rows <= 0) return ORC_BAD_SHAPE;
+    for (int64_t mi = 0; mi < m; ++mi) {
+        int64_t best = 0;
+        for (int64_t r = 1; r < rows; ++r)
+            if (y[mi * rows + r] > y[mi * rows + best]) best = r;
+        idx[mi] = best;
+    }
+    return ORC_OK;
+}
