@@ -265,6 +265,42 @@ TERN_API tern_status tern_gemm_batched_rmsnorm(const tern_batch_item *items, con
  * streams, or a captured graph replayed beside another call) race on it. */
 TERN_API tern_status tern_gemm_batched_noalloc(const tern_batch_item *items, int32_t n, void *stream);
 
+/* An int8 matrix with per-row scales: the output head of the model page
+ * ("Where the bytes live": a 151,936 x 4,096 int8 head, scaled per row).
+ * w: rows * k int8, row-major, 16-byte aligned; scale: rows fp32. */
+typedef struct {
+    int32_t rows;        /* R >= 1 */
+    int32_t k;           /* K >= 64, K % 64 == 0 */
+    const int8_t *w;     /* R * K */
+    const float *scale;  /* R */
+} tern_i8_matrix;
+
+/* Output head with the greedy choice fused (model page: the int8 head, read
+ * once per generated token, and the speculative verifier's greedy
+ * acceptance): for each activation row i < m,
+ *     logits[i][r] = scale[r] * sum_k w[r][k] * x[i][k]      (fp32)
+ *     argmax[i]    = the r of the largest logits[i][r], the lowest r on ties,
+ * where the argmax is taken over the fp32 logits this call writes.  With
+ * norm_w != NULL each x row is first normalised as in
+ * tern_gemm_batched_rmsnorm (the final norm ahead of the head).
+ * x: [m][k] bf16, 16-byte aligned; logits: [m][rows] fp32, 4-byte aligned;
+ * argmax: m int32, 4-byte aligned; norm_w: NULL or k fp32, 16-byte aligned.
+ * 1 <= m <= TERN_MAX_M, m * k * 2 <= TERN_MAX_X_BYTES.
+ * Arithmetic: each weight enters the tensor cores as two exact e4m3 nibble
+ * terms and x as e4m3 terms as in the ternary products, so the logits are
+ * fp32 sums of exact products; their error is a few fp32 roundings of
+ * sum_k |w x| (not of the logit itself).
+ * Launches: a 1-thread-block kernel that resets the argmax state, the
+ * activation-preparing kernel when m >= 2, the persistent kernel, and a
+ * 1-thread-block kernel that writes argmax.  Workspace: as tern_gemm_batched,
+ * plus 64 bytes per (context, stream) for the argmax state.
+ * Errors: TERN_ERR_NULL, TERN_ERR_SHAPE (rows < 1, k < 64, k % 64, m * k * 2
+ * over the limit), TERN_ERR_M_RANGE, TERN_ERR_ALIGN, TERN_ERR_VALUE (eps),
+ * TERN_ERR_CUDA. */
+TERN_API tern_status tern_lmhead_argmax(const tern_i8_matrix *w, const uint16_t *x, int32_t m,
+                                        const float *norm_w, float eps, float *logits, int32_t *argmax,
+                                        void *stream);
+
 /* Synchronise `stream`, then report and clear the device error word that
  * bounded device-side waits set when they run out (TERN_ERR_TIMEOUT), or a
  * pending CUDA error (TERN_ERR_CUDA).  TERN_OK otherwise. */

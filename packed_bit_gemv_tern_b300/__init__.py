@@ -38,7 +38,7 @@ TERN_NOALLOC_WS_BYTES = 4194304
 ABI_FUNCTIONS = (
     "tern_pack", "tern_validate", "tern_unpack", "tern_gemv", "tern_gemv_swiglu",
     "tern_gemm_smallm", "tern_gemm_smallm_swiglu", "tern_gemm_batched", "tern_gemm_batched_launches",
-    "tern_gemm_batched_noalloc", "tern_gemm_batched_rmsnorm",
+    "tern_gemm_batched_noalloc", "tern_gemm_batched_rmsnorm", "tern_lmhead_argmax",
     "tern_last_device_error", "tern_set_wait_limit",
     "tern_status_str", "tern_abi_version",
 )
@@ -53,6 +53,10 @@ class TernError(RuntimeError):
 class CMatrix(ctypes.Structure):
     _fields_ = [("rows", ctypes.c_int32), ("k", ctypes.c_int32), ("codes", ctypes.c_void_p),
                 ("scale", ctypes.c_void_p), ("rowsum", ctypes.c_void_p)]
+
+
+class CI8Matrix(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int32), ("k", ctypes.c_int32), ("w", ctypes.c_void_p), ("scale", ctypes.c_void_p)]
 
 
 class CBatchItem(ctypes.Structure):
@@ -88,6 +92,7 @@ def load(path: str | None = None):
             "tern_gemm_batched_launches": [vp, i32],
             "tern_gemm_batched_noalloc": [vp, i32, vp],
             "tern_gemm_batched_rmsnorm": [vp, vp, ctypes.c_float, i32, vp],
+            "tern_lmhead_argmax": [vp, vp, i32, vp, ctypes.c_float, vp, vp, vp],
             "tern_last_device_error": [vp],
             "tern_set_wait_limit": [ctypes.c_int64],
             "tern_status_str": [ctypes.c_int],
@@ -178,6 +183,31 @@ class TernMatrix:
         return ctypes.byref(self._c)
 
 
+class I8Matrix:
+    """An int8 matrix with per-row fp32 scales resident on the GPU (the
+    output head); torch tensors own the memory."""
+
+    def __init__(self, w, scale):
+        self.w = w            # torch.int8 [rows, k]
+        self.scale = scale    # torch.float32 [rows]
+        self.rows, self.k = int(w.shape[0]), int(w.shape[1])
+        self._c = CI8Matrix(self.rows, self.k, w.data_ptr() if w.numel() else None,
+                            scale.data_ptr() if scale.numel() else None)
+
+    @classmethod
+    def from_host(cls, w: np.ndarray, scale: np.ndarray, device="cuda"):
+        import torch
+        return cls(torch.from_numpy(np.ascontiguousarray(w, np.int8)).to(device),
+                   torch.from_numpy(np.ascontiguousarray(scale, np.float32)).to(device))
+
+    @property
+    def packed_bytes(self) -> int:
+        return self.rows * self.k
+
+    def ref(self):
+        return ctypes.byref(self._c)
+
+
 def _stream_handle(stream):
     import torch
     if stream is None:
@@ -254,6 +284,13 @@ def tern_gemm_batched_rmsnorm(items, norm_w, eps: float = 1e-6, stream=None):
     _check(load().tern_gemm_batched_rmsnorm(ctypes.cast(arr, ctypes.c_void_p) if len(arr) else None,
                                             ctypes.cast(ptrs, ctypes.c_void_p), ctypes.c_float(eps), len(arr),
                                             _stream_handle(stream)), "tern_gemm_batched_rmsnorm")
+
+
+def tern_lmhead_argmax(w: I8Matrix, x, m: int, logits, argmax, norm_w=None, eps: float = 1e-6, stream=None):
+    """Output-head logits [m, rows] and the per-row greedy choice argmax [m]
+    (int32 tensor), with an optional RMSNorm of x first."""
+    _check(load().tern_lmhead_argmax(w.ref(), _dptr(x), int(m), _dptr(norm_w), ctypes.c_float(eps), _dptr(logits),
+                                     _dptr(argmax), _stream_handle(stream)), "tern_lmhead_argmax")
 
 
 def tern_gemm_batched_launches(items) -> int:

@@ -78,6 +78,21 @@ constexpr uint32_t kTmemCols = 512;
 // the four 128-code columns q of a stage.  N = 32 (m >= 5): D[buf][q] at
 // kDCol + 32 * (2 buf + q) for two 256-code columns.
 constexpr uint32_t kDCol = kASlots * 128;
+// Weight formats of the persistent kernel: the ternary 2-bit codes (a stage
+// is 512 codes of a row, 32 activation words of 16), and the int8 output
+// head (a stage is 128 weights of a row, 8 activation words).  For int8 each
+// weight b = 16 (h - 8) + l with h, l in [0, 15] (offset binary), and both
+// nibbles enter the MMA as e4m3 bytes whose value is nibble * 2^-9 (the
+// e4m3 bytes 0x00..0x0F are exactly v * 2^-9): TMEM slot g holds the l
+// bytes of a stage in columns 64g .. 64g + 31 and the h bytes in 64g + 32 ..
+// 64g + 63, and each of the four chunk columns (one K = 32 step each) has
+// an accumulator per nibble, D_l[buf][q] at kDColL + 16 (4 buf + q) and
+// D_h at kDColH + 16 (4 buf + q).
+constexpr int kFmtTern = 0;
+constexpr int kFmtI8 = 1;
+constexpr uint32_t kDColL = 256;
+constexpr uint32_t kDColH = 384;
+__host__ __device__ constexpr int stage_b_words(int fmt) { return fmt == kFmtI8 ? 8 : kStageWords; }
 // Two B buffers, contiguous, then the MMA's read slack.  A chunk is planned
 // so that its one-band operand (b_block_bytes(m, 1) per 16-code block) fits
 // one buffer; a chunk that needs two bands (twice the bytes) takes both
@@ -118,6 +133,7 @@ struct Params {
     int n_items;
     float eps;                     // RMSNorm eps of the items with norm weights
     long long wait_limit;          // bound of every Waiter, in cycles
+    unsigned long long *keys;      // int8 head: per activation row the best (logit, index) key so far
     int unit_start[kMaxCtas + 1];  // CTA b runs units [unit_start[b], unit_start[b + 1])
     int item_start[kMaxCtas];      // the item holding unit unit_start[b]
     int stages_cta[kMaxCtas];      // 512-code stages in CTA b's run
@@ -147,9 +163,10 @@ constexpr uint32_t kWordsOff = kBarTurn + 8 * kCols * kDecGroups;
 // [40..71] buffer 1's: per activation row i, [2i] row maximum and [2i + 1]
 // band-B maximum; [16] the chunk's number times 4 plus its band count; [17],
 // [18] scratch of the m = 1 build; [24 + i] row i's RMSNorm factor (fp32
-// bits; items with a norm)
-constexpr uint32_t kWordsCount = 72;
-constexpr uint32_t kXmWords = 32;
+// bits; items with a norm); [32 + 2i], [33 + 2i] the chunk's sum of row i's
+// activations as an fp32 pair (int8 head)
+constexpr uint32_t kWordsCount = 104;
+constexpr uint32_t kXmWords = 48;
 constexpr uint32_t kSmemBytes = 1024 + kOffBar + kWordsOff + kWordsCount * 4;
 
 __device__ unsigned int g_batched_error;
@@ -217,14 +234,18 @@ struct Cursor {
 constexpr int kPrepThreads = 128;
 constexpr int kPrepWords = 7;           // words per thread: 28 stages * 32 / 128
 constexpr uint32_t kBulkPiece = 16384;  // bytes per bulk copy of a prepared chunk
-// Per-chunk metadata (32 words): for activation row i, [2i] its maximum and
+// Per-chunk metadata (48 words): for activation row i, [2i] its maximum and
 // [2i + 1] its band-B maximum (fp32 bits of |x|), [16 + i] 1 if it needs
-// band B, [24 + i] its RMSNorm factor (items with a norm).
-constexpr int kMetaWords = 32;
+// band B, [24 + i] its RMSNorm factor (items with a norm), [32 + 2i] and
+// [33 + 2i] the sum of its activations over the chunk as an fp32 pair (int8
+// head).
+constexpr int kMetaWords = 48;
 
 struct PrepItem {
     const uint16_t *x;
     const float *norm_w;  // RMSNorm channel weights [k], or nullptr
+    int sw;               // activation words per stage (stage_b_words)
+    int head;             // int8 head: B in k order, and the chunk's activation sums
     unsigned char *b;
     uint32_t *meta;
     int k, m, stages, cstages;
@@ -266,8 +287,8 @@ __global__ void __launch_bounds__(kPrepThreads) k_tern_bprep(const __grid_consta
     while (j + 1 < p.n_items && p.item[j + 1].task0 <= task) ++j;
     const PrepItem &it = p.item[j];
     const int local = task - it.task0, c = local / it.m, mm = local - c * it.m;
-    const int w0 = c * it.cstages * kStageWords;
-    const int nw = min(it.cstages, it.stages - c * it.cstages) * kStageWords;
+    const int w0 = c * it.cstages * it.sw;
+    const int nw = min(it.cstages, it.stages - c * it.cstages) * it.sw;
     const int kw = it.k / 16;
     const uint4 *xr = reinterpret_cast<const uint4 *>(it.x + (size_t)mm * it.k);  // 2 x uint4 per word
     uint4 va[kPrepWords], vb[kPrepWords];
@@ -332,6 +353,24 @@ __global__ void __launch_bounds__(kPrepThreads) k_tern_bprep(const __grid_consta
         n += stat[w][1];
         sabs += __uint_as_float(stat[w][2]);
     }
+    if (it.head) {
+        double sx = 0.0;
+#pragma unroll
+        for (int q = 0; q < kPrepWords; ++q) sx += sum16(va[q], vb[q]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sx += __shfl_xor_sync(0xFFFFFFFFu, sx, o);
+        __syncthreads();  // ssred free
+        if ((tid & 31) == 0) ssred[tid >> 5] = sx;
+        __syncthreads();
+        if (tid == 0) {
+            sx = 0.0;
+            for (int w = 0; w < kPrepThreads / 32; ++w) sx += ssred[w];
+            const float hi = (float)sx;
+            uint32_t *meta = it.meta + (size_t)kMetaWords * c;
+            meta[32 + 2 * mm] = __float_as_uint(hi);
+            meta[33 + 2 * mm] = __float_as_uint((float)(sx - (double)hi));
+        }
+    }
     if (tid == 0) {
         uint32_t *meta = it.meta + (size_t)kMetaWords * c;
         meta[2 * mm] = ma;
@@ -347,7 +386,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_tern_bprep(const __grid_consta
         const int wi = tid + q * kPrepThreads;
         if (wi < nw) {
             uint4 rows[2];
-            split_word1(va[q], vb[q], sc, rows);
+            split_word1(va[q], vb[q], sc, rows, it.head != 0);
             uint4 *d = reinterpret_cast<uint4 *>(dst + (size_t)wi * wbytes);
             d[0] = rows[0];
             d[1] = rows[1];
@@ -377,9 +416,61 @@ __device__ __noinline__ void issue_two_band(uint32_t tmem, uint32_t bbuf, int g,
                               (st != 0 || t != 0) ? 1u : 0u);
 }
 
+// int8 head: the MMAs of one stage's column `quad` for a chunk with two
+// bands (N = 16 for m <= 4 with four one-step columns; N = 32 for m >= 5 with
+// two two-step columns issued by quads 0 and 1), both nibbles of each step.
+__device__ __noinline__ void issue_two_band_i8(uint32_t tmem, uint32_t bbuf, int g, int quad, int buf, int st, int m)
+{
+    const int n = mma_n(m, 2);
+    const int cols = n == 32 ? 2 : kCols;
+    if (quad >= cols) return;
+    const int steps = 4 / cols;  // K = 32 steps per column
+    const uint32_t wbytes = b_block_bytes(m, 2);
+    const uint32_t idesc = idesc_n(n);
+    const uint32_t dl = tmem + kDColL + (uint32_t)(n * (cols * buf + quad)), dh = dl + (kDColH - kDColL);
+    for (int t = 0; t < steps; ++t) {
+        const int ks = quad * steps + t;
+        const uint32_t al = tmem + (uint32_t)(g * 64 + 8 * ks);
+        const uint64_t bd = b_desc_lbo(bbuf + (uint32_t)(st * stage_b_words(kFmtI8) + 2 * ks) * wbytes, wbytes);
+        const uint32_t acc = (st != 0 || t != 0) ? 1u : 0u;
+        ptx::mma_ts_f8f6f4_lh(dl, al, (uint32_t)bd, (uint32_t)(bd >> 32), idesc, acc);
+        ptx::mma_ts_f8f6f4_lh(dh, al + 32u, (uint32_t)bd, (uint32_t)(bd >> 32), idesc, acc);
+    }
+}
+
+// One stage of one int8 row (128 weights in 8 words, after the swizzle) ->
+// its TMEM A rows: the low nibbles l = b & 15 in the first 32 columns, the
+// offset high nibbles h = ((b ^ 0x80) >> 4) in the next 32, each as the e4m3
+// byte of value nibble * 2^-9.
+__device__ __forceinline__ void decode_i8_stage(uint32_t srow, uint32_t sw, uint32_t ta)
+{
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {  // 64 weights: TMEM columns 16 half .. 16 half + 15 of each nibble
+        uint32_t w[16];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            const uint4 v = ptx::lds128(srow + ((((uint32_t)(4 * half + c)) ^ sw) << 4));
+            w[4 * c] = v.x;
+            w[4 * c + 1] = v.y;
+            w[4 * c + 2] = v.z;
+            w[4 * c + 3] = v.w;
+        }
+        uint32_t r[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) r[j] = w[j] & 0x0F0F0F0Fu;
+        ptx::tmem_st_32x32b_x16(ta + 16u * (uint32_t)half, r);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) r[j] = ((w[j] >> 4) ^ 0x08080808u) & 0x0F0F0F0Fu;
+        ptx::tmem_st_32x32b_x16(ta + 32u + 16u * (uint32_t)half, r);
+    }
+}
+
+template <int kFmt>
 __global__ void __launch_bounds__(kThreads, 1)
 k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps maps)
 {
+    constexpr bool kI8 = kFmt == kFmtI8;
+    constexpr int kSW = stage_b_words(kFmt);  // activation words per stage
     extern __shared__ unsigned char smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -518,14 +609,18 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                 if (__all_sync(0xFFFFFFFFu, okw && oka)) {
                     ptx::tc_fence_after();
                     const uint32_t srow = row_addr + (uint32_t)w_r * kStageBytes;
-                    const uint32_t ta = tm_row + (uint32_t)(g * 128);
+                    if constexpr (kI8) {
+                        decode_i8_stage(srow, sw, tm_row + (uint32_t)(g * 64));
+                    } else {
+                        const uint32_t ta = tm_row + (uint32_t)(g * 128);
 #pragma unroll 1
-                    for (int c = 0; c < 4; ++c) {
-                        const uint4 v0 = ptx::lds128(srow + ((((uint32_t)(2 * c)) ^ sw) << 4));
-                        const uint4 v1 = ptx::lds128(srow + ((((uint32_t)(2 * c + 1)) ^ sw) << 4));
-                        uint32_t r[32];
-                        decode8(v0, v1, r);
-                        ptx::tmem_st_32x32b_x32(ta + 32u * (uint32_t)c, r);
+                        for (int c = 0; c < 4; ++c) {
+                            const uint4 v0 = ptx::lds128(srow + ((((uint32_t)(2 * c)) ^ sw) << 4));
+                            const uint4 v1 = ptx::lds128(srow + ((((uint32_t)(2 * c + 1)) ^ sw) << 4));
+                            uint32_t r[32];
+                            decode8(v0, v1, r);
+                            ptx::tmem_st_32x32b_x32(ta + 32u * (uint32_t)c, r);
+                        }
                     }
                     ptx::mbar_arrive(bars + kBarWEmpty + 8 * w_r);  // after the last store, which consumed the loads
                     ptx::tmem_wait_st();
@@ -560,7 +655,25 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                             bw = words[8 + kXmWords * buf + 16];
                             bw_gc = gc;
                         }
-                        if ((bw & 3u) != 2u) {
+                        if constexpr (kI8) {
+                            if ((bw & 3u) != 2u) {
+                                // one band, N = 16: column q is K step q of the
+                                // stage, one MMA per nibble
+                                const uint32_t wbytes = b_block_bytes(m, 1);
+                                const uint32_t dl = tmem + kDColL + 16u * (uint32_t)(kCols * buf + quad);
+                                const uint32_t al = tmem + (uint32_t)(g * 64 + 8 * quad);
+                                const uint64_t bd = b_desc_lbo(bbuf + (uint32_t)buf * kBBufBytes +
+                                                                   (uint32_t)(st * kSW + 2 * quad) * wbytes,
+                                                               wbytes);
+                                constexpr uint32_t kIdesc16 = idesc_n(16);
+                                const uint32_t acc = st != 0 ? 1u : 0u;
+                                ptx::mma_ts_f8f6f4_lh(dl, al, (uint32_t)bd, (uint32_t)(bd >> 32), kIdesc16, acc);
+                                ptx::mma_ts_f8f6f4_lh(dl + (kDColH - kDColL), al + 32u, (uint32_t)bd,
+                                                      (uint32_t)(bd >> 32), kIdesc16, acc);
+                            } else {
+                                issue_two_band_i8(tmem, bbuf, g, quad, buf, st, m);
+                            }
+                        } else if ((bw & 3u) != 2u) {
                             // one band: N = 16 (2m <= 16); compact B, column q
                             // of stage st at word st*32 + 8q, its K = 32 step t
                             // at A column +8t and B word +2t
@@ -634,7 +747,108 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
         // unit if it was its last chunk.  Within a band the issuing columns
         // and the hi/lo terms are summed in fp32 (one band, one scale); each
         // band's total then goes into the row's pair.
+        // int8 head: chunk e's two accumulators per column, the offset
+        // removed with the chunk's activation sums, the unit's logits written
+        // and each warp's best (logit, lowest row) merged into p.keys.
+        auto epilogue_i8 = [&](int e) {
+            const int eb = e & 1;
+            const Item &it = p.item[prev_item];
+            const uint32_t *xm = meta_s + kXmWords * eb;
+            const int bands = (int)(xm[16] & 3u);
+            const int n = mma_n(it.m, bands), cols = n == 32 ? 2 : kCols;
+            uint32_t good = 1u;
+            if (lane == 0) good = waiter.wait(bars + kBarDFull + 8 * eb, (e >> 1) & 1) ? 1u : 0u;
+            good = __shfl_sync(0xFFFFFFFFu, good, 0);
+            if (good) {
+                ptx::tc_fence_after();
+                const uint32_t bl = tmem + ((uint32_t)(quad * 32) << 16) + kDColL + (uint32_t)(n * cols * eb);
+                const uint32_t bh = bl + (kDColH - kDColL);
+                // per activation row: both nibbles' sums, b = 16 (h - 8) + l,
+                // so sum b x = 2^13 sum h' x + 2^9 sum l' x - 128 sum x where
+                // h' = h 2^-9 and l' = l 2^-9 are the MMA's A values
+                for (int h = 0; h < 2 && 16 * h < 2 * bands * it.m; ++h) {
+                    float dl[16], dh[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) dl[q] = dh[q] = 0.f;
+                    for (int c = 0; c < cols; ++c) {
+                        uint32_t vl[16], vh[16];
+                        ptx::tmem_ld_32x32b_x16(bl + (uint32_t)(n * c + 16 * h), vl);
+                        ptx::tmem_ld_32x32b_x16(bh + (uint32_t)(n * c + 16 * h), vh);
+                        ptx::tmem_wait_ld();
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) {
+                            dl[q] += __uint_as_float(vl[q]);
+                            dh[q] += __uint_as_float(vh[q]);
+                        }
+                    }
+                    if (bands == 1) {  // column 2i: hi, 2i + 1: lo term of row i
+#pragma unroll
+                        for (int mm = 0; mm < 8; ++mm) {
+                            if (mm < it.m) {
+                                const int sa = row_scale_exp(xm[2 * mm]);
+                                const float fa = exp2i(-sa), fb = exp2i(-sa - 4);
+                                acc_pair(acc[mm], acc_lo[mm], 8192.f * fmaf(dh[2 * mm + 1], fb, dh[2 * mm] * fa));
+                                acc_pair(acc[mm], acc_lo[mm], 512.f * fmaf(dl[2 * mm + 1], fb, dl[2 * mm] * fa));
+                            }
+                        }
+                    } else {  // column 4i + b: hi_A, lo_A, hi_B, lo_B of row i
+#pragma unroll
+                        for (int r = 0; r < 4; ++r) {
+                            const int mm = 4 * h + r;
+                            if (mm < it.m) {
+                                const int sa = row_scale_exp(xm[2 * mm]), sb = row_scale_exp(xm[2 * mm + 1]);
+                                const float fa = exp2i(-sa), fa4 = exp2i(-sa - 4), fb = exp2i(-sb), fb4 = exp2i(-sb - 4);
+                                acc_pair(acc[mm], acc_lo[mm], 8192.f * fmaf(dh[4 * r + 1], fa4, dh[4 * r] * fa));
+                                acc_pair(acc[mm], acc_lo[mm], 8192.f * fmaf(dh[4 * r + 3], fb4, dh[4 * r + 2] * fb));
+                                acc_pair(acc[mm], acc_lo[mm], 512.f * fmaf(dl[4 * r + 1], fa4, dl[4 * r] * fa));
+                                acc_pair(acc[mm], acc_lo[mm], 512.f * fmaf(dl[4 * r + 3], fb4, dl[4 * r + 2] * fb));
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int mm = 0; mm < 8; ++mm) {
+                    if (mm < it.m) {
+                        acc_pair(acc[mm], acc_lo[mm], -128.f * __uint_as_float(xm[32 + 2 * mm]));
+                        acc_pair(acc[mm], acc_lo[mm], -128.f * __uint_as_float(xm[33 + 2 * mm]));
+                    }
+                }
+            }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bars + kBarDEmpty + 8 * eb);
+            if (!prev_last) return;
+            const int r = prev_tile * 128 + i;
+            const bool live = r < it.rows;
+            const float sc = live ? it.scale_g[r] : 0.f;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                if (q < it.m) {
+                    float yv = sc * __fadd_rn(acc[q], acc_lo[q]);
+                    if (yv == 0.f) yv = 0.f;  // one zero for the order below
+                    if (live) it.y[(size_t)q * it.rows + r] = yv;
+                    // order-preserving bits of the logit, then the inverted row:
+                    // the largest key is the largest logit at the lowest row
+                    const uint32_t u = __float_as_uint(yv);
+                    const uint32_t ou = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+                    unsigned long long key = live ? ((unsigned long long)ou << 32) | (unsigned long long)(~(uint32_t)r) : 0ull;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        const unsigned long long other = __shfl_xor_sync(0xFFFFFFFFu, key, o);
+                        key = other > key ? other : key;
+                    }
+                    if (lane == 0 && key != 0ull) atomicMax(p.keys + q, key);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = acc_lo[q] = 0.f;
+        };
+
         auto epilogue = [&](int e) {
+            if constexpr (kI8) {
+                epilogue_i8(e);
+                return;
+            }
             const int eb = e & 1;
             const Item &it = p.item[prev_item];
             const uint32_t *xm = meta_s + kXmWords * eb;
@@ -778,7 +992,7 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                 }
                 uint4 rows[4];
                 split_word2(va, vb, exp2i(row_scale_exp(xm[2 * mm])), exp2i(row_scale_exp(xm[2 * mm + 1])),
-                            band_threshold2(xm[2 * mm]), rows);
+                            band_threshold2(xm[2 * mm]), rows, kI8);
                 const uint32_t at = bbuf + (uint32_t)wi * wbytes + 64u * (uint32_t)mm;
 #pragma unroll
                 for (int r = 0; r < 4; ++r) ptx::sts128(at + 16u * (uint32_t)r, rows[r]);
@@ -803,8 +1017,8 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
             const uint32_t bfull = bars + kBarBFull + 8 * buf;
             if (!reuse) {
                 const int m = it.m;
-                const int n_words = cur.n_stages_chunk * kStageWords;
-                const int w0 = cur.chunk * cur.cstages * kStageWords;
+                const int n_words = cur.n_stages_chunk * kSW;
+                const int w0 = cur.chunk * cur.cstages * kSW;
                 if (it.bsrc != nullptr) {
                     // prepared: the rows' maxima and band-B flags; with one
                     // band the chunk's bytes in a few bulk copies that complete
@@ -816,6 +1030,9 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                     bands = __any_sync(0xFFFFFFFFu, flag != 0u) ? 2 : 1;
                     if (st_tid < 2 * m) xm[st_tid] = meta[st_tid];
                     if (it.norm_w != nullptr && st_tid < m) xm[24 + st_tid] = meta[24 + st_tid];
+                    if constexpr (kI8) {
+                        if (st_tid < 2 * m) xm[32 + st_tid] = meta[32 + st_tid];
+                    }
                     if (bands == 1) {
                         if (st_tid == 0) {
                             const uint32_t bytes = (uint32_t)n_words * b_block_bytes(m, 1);
@@ -881,17 +1098,43 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                     }
                     ptx::cp_async_wait_all();
                     ptx::named_bar_sync(1, kStagers);
-                    for (int wi = st_tid; wi < n_words; wi += kStagers) {
+                    double sx = 0.0;  // int8 head: the chunk's activation sum
+                    // (every staging thread takes the same number of turns
+                    // through the loops with warp reductions: a chunk's word
+                    // count need not be a multiple of 32; past it, zeros)
+                    for (int base = 0; base < n_words; base += kStagers) {
+                        const int wi = base + st_tid;
                         const uint32_t at = bb + 32u * (uint32_t)wi;
-                        const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, max_abs16(ptx::lds128(at), ptx::lds128(at + 16u)));
+                        const bool in = wi < n_words;
+                        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                        const uint4 va = in ? ptx::lds128(at) : z, vb = in ? ptx::lds128(at + 16u) : z;
+                        const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, max_abs16(va, vb));
                         if (lane == 0) atomicMax(&xm[0], mx);
+                        if constexpr (kI8) sx += sum16(va, vb);
+                    }
+                    if constexpr (kI8) {
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) sx += __shfl_xor_sync(0xFFFFFFFFu, sx, o);
+                        if (lane == 0) reinterpret_cast<double *>(xch)[4 + quad] = sx;
                     }
                     ptx::named_bar_sync(1, kStagers);
+                    if constexpr (kI8) {
+                        if (st_tid == 0) {
+                            const double *d = reinterpret_cast<const double *>(xch) + 4;
+                            const double t = d[0] + d[1] + d[2] + d[3];
+                            const float hi = (float)t;
+                            xm[32] = __float_as_uint(hi);
+                            xm[33] = __float_as_uint((float)(t - (double)hi));
+                        }
+                    }
                     const uint32_t tb2 = band_threshold2(xm[0]);
                     const float sca = exp2i(row_scale_exp(xm[0]));
-                    for (int wi = st_tid; wi < n_words; wi += kStagers) {
+                    for (int base = 0; base < n_words; base += kStagers) {
+                        const int wi = base + st_tid;
                         const uint32_t at = bb + 32u * (uint32_t)wi;
-                        const uint4 va = ptx::lds128(at), vb = ptx::lds128(at + 16u);
+                        const bool in = wi < n_words;
+                        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                        const uint4 va = in ? ptx::lds128(at) : z, vb = in ? ptx::lds128(at + 16u) : z;
                         uint32_t cnt = 0;
                         float sa = 0.f;
                         band_stats16(va, vb, tb2, cnt, sa);
@@ -904,10 +1147,12 @@ k_tern_batched(const __grid_constant__ Params p, const __grid_constant__ Maps ma
                             atomicAdd(&xm[17], cnt);
                             atomicAdd(sabs, sa);
                         }
-                        uint4 rows[2];
-                        split_word1(va, vb, sca, rows);
-                        ptx::sts128(at, rows[0]);
-                        ptx::sts128(at + 16u, rows[1]);
+                        if (in) {
+                            uint4 rows[2];
+                            split_word1(va, vb, sca, rows, kI8);
+                            ptx::sts128(at, rows[0]);
+                            ptx::sts128(at + 16u, rows[1]);
+                        }
                     }
                     ptx::named_bar_sync(1, kStagers);
                     bands = need_two_bands(xm[0], xm[17], *sabs) ? 2 : 1;
@@ -999,14 +1244,15 @@ std::vector<int> plan_groups(const tern_batch_item *items, int n)
 // A grown-out buffer is never freed: a launch captured in a CUDA graph keeps
 // the address it was captured with.  Returns nullptr if the allocation fails
 // (the call then returns TERN_ERR_CUDA; the groups before it have launched).
-void *workspace(cudaStream_t stream, size_t need)
+void *workspace(cudaStream_t stream, size_t need, int slot = 0)
 {
     struct Buf {
         void *p = nullptr;
         size_t bytes = 0;
     };
     static std::mutex mu;
-    static std::map<std::pair<unsigned long long, cudaStream_t>, Buf> all;
+    static std::map<std::pair<unsigned long long, cudaStream_t>, Buf> all_slots[2];  // 0: prepared B, 1: head keys
+    auto &all = all_slots[slot];
     // keyed by the current context: a context created after a device reset
     // gets buffers of its own
     const unsigned long long ctx = current_context_id();
@@ -1035,20 +1281,23 @@ size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 // 512-code stages over K, and stages per chunk: the fewest chunks that fit a
 // B buffer, of equal stage counts (a short last chunk would pay the
 // per-chunk costs for little work).
-void chunk_plan(int k, int m, int &stages, int &cstages)
+void chunk_plan(int k, int m, int &stages, int &cstages, int sw = kStageWords)
 {
-    stages = (k / 16 + kStageWords - 1) / kStageWords;
-    const int cap = kBBufBytes / (kStageWords * (int)b_block_bytes(m, 1));  // stages of one-band B one buffer holds
+    stages = (k / 16 + sw - 1) / sw;
+    const int cap = kBBufBytes / (sw * (int)b_block_bytes(m, 1));  // stages of one-band B one buffer holds
     const int n_chunks = (stages + cap - 1) / cap;
     cstages = (stages + n_chunks - 1) / n_chunks;
 }
 
 // Workspace bytes of one prepared item (see Item::bsrc, Item::meta).
-size_t prep_b_bytes(int stages, int m) { return align256((size_t)stages * kStageWords * b_block_bytes(m, 1)); }
-size_t prep_bytes(int stages, int cstages, int m)
+size_t prep_b_bytes(int stages, int m, int sw = kStageWords)
+{
+    return align256((size_t)stages * sw * b_block_bytes(m, 1));
+}
+size_t prep_bytes(int stages, int cstages, int m, int sw = kStageWords)
 {
     const int n_chunks = (stages + cstages - 1) / cstages;
-    return prep_b_bytes(stages, m) + align256((size_t)n_chunks * kMetaWords * sizeof(uint32_t));
+    return prep_b_bytes(stages, m, sw) + align256((size_t)n_chunks * kMetaWords * sizeof(uint32_t));
 }
 
 // Scratch of tern_gemm_batched_noalloc: module-scope device memory, which the
@@ -1080,14 +1329,28 @@ int batched_launches(const tern_batch_item *items, int n)
 
 namespace {
 
-// Launches the batch.  fixed_ws: a workspace the caller guarantees to be
-// large enough for every launch group (nullptr: the per-stream workspace).
-// norm_w: nullptr, or per item the RMSNorm channel weights (nullptr for an
-// item without a norm), with eps.
-tern_status run_batched(const tern_batch_item *items, int n, cudaStream_t stream, unsigned char *fixed_ws,
-                        const float *const *norm_w = nullptr, float eps = 0.f)
+// One product of a launch group, in the form the launch needs.  codes_*:
+// the weights as uint32 words, kw per row (16 ternary codes or 4 int8
+// weights a word).
+struct Job {
+    const uint32_t *codes_g, *codes_u;  // codes_u: the up projection of a SwiGLU pair, or nullptr
+    const float *scale_g, *scale_u;
+    const uint16_t *x;
+    float *y;
+    const float *norm_w;
+    int rows, k, m, kw;
+};
+
+// Launches one group (cnt jobs, each with rows > 0 and k > 0): the preparing
+// kernel if some job has m >= 2, then the persistent kernel of format kFmt.
+// fixed_ws: a workspace the caller guarantees to be large enough (nullptr:
+// the per-stream workspace).  keys: the int8 head's argmax keys.
+template <int kFmt>
+tern_status launch_group(const Job *jobs, int cnt, cudaStream_t stream, unsigned char *fixed_ws, float eps,
+                         unsigned long long *keys)
 {
     static_assert(sizeof(Params) + sizeof(Maps) < 32000, "kernel parameters exceed 32 KB");
+    constexpr int kSW = stage_b_words(kFmt);
     const int sms = sm_count();
     // the kernel's shared-memory attribute, once per context (a context
     // created after a device reset starts without it)
@@ -1097,20 +1360,145 @@ tern_status run_batched(const tern_batch_item *items, int n, cudaStream_t stream
         const unsigned long long ctx = current_context_id();
         std::lock_guard<std::mutex> lock(mu);
         if (ctx == 0 || done.count(ctx) == 0) {
-            if (cudaFuncSetAttribute(k_tern_batched, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes) !=
-                cudaSuccess)
+            if (cudaFuncSetAttribute(k_tern_batched<kFmt>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kSmemBytes) != cudaSuccess)
                 return TERN_ERR_CUDA;
             if (ctx != 0) done.insert(ctx);
         }
     }
+    Params prm;
+    std::memset(&prm, 0, sizeof(prm));
+    Maps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    std::vector<long long> unit_cost;
+    int units = 0, n_maps = 0;
+    for (int j = 0; j < cnt; ++j) {
+        const Job &b = jobs[j];
+        Item &it = prm.item[j];
+        it.scale_g = b.scale_g;
+        it.scale_u = b.scale_u;
+        it.x = b.x;
+        it.y = b.y;
+        it.rows = b.rows;
+        it.k = b.k;
+        it.m = b.m;
+        it.swiglu = b.codes_u != nullptr;
+        it.norm_w = b.norm_w;
+        chunk_plan(it.k, it.m, it.stages, it.cstages, kSW);
+        it.unit0 = units;
+        it.map = n_maps;
+        const int tile_rows = it.swiglu ? 64 : 128;
+        const int tiles = (it.rows + tile_rows - 1) / tile_rows;
+        if (!make_code_map(&maps.m[n_maps++], b.codes_g, it.rows, b.kw, tile_rows)) return TERN_ERR_CUDA;
+        if (it.swiglu && !make_code_map(&maps.m[n_maps++], b.codes_u, it.rows, b.kw, tile_rows))
+            return TERN_ERR_CUDA;
+        for (int t = 0; t < tiles; ++t) unit_cost.push_back(it.stages);
+        units += tiles;
+    }
+    prm.n_items = cnt;
+    prm.eps = eps;
+    prm.wait_limit = wait_limit();
+    prm.keys = keys;
+
+    // Items with m >= 2 take their B from the workspace, written by one
+    // k_tern_bprep launch just before (one CTA per item, K chunk and
+    // activation row): per item the padded K's one-band words (32m bytes
+    // per 16 activations), then kMetaWords of metadata per chunk.  Items
+    // with m = 1 are built by the persistent kernel's staging warps.
+    PrepParams pp;
+    std::memset(&pp, 0, sizeof(pp));
+    pp.eps = eps;
+    size_t ws_need = 0;
+    std::vector<std::pair<size_t, size_t>> ws_off(cnt);
+    for (int j = 0; j < cnt; ++j) {
+        const Item &it = prm.item[j];
+        if (it.m < 2) continue;
+        ws_off[j].first = ws_need;
+        ws_off[j].second = ws_need + prep_b_bytes(it.stages, it.m, kSW);
+        ws_need += prep_bytes(it.stages, it.cstages, it.m, kSW);
+    }
+    if (ws_need > 0) {
+        unsigned char *ws = fixed_ws != nullptr ? fixed_ws : static_cast<unsigned char *>(workspace(stream, ws_need));
+        if (ws == nullptr) return TERN_ERR_CUDA;
+        for (int j = 0; j < cnt; ++j) {
+            Item &it = prm.item[j];
+            if (it.m < 2) continue;
+            it.bsrc = ws + ws_off[j].first;
+            it.meta = reinterpret_cast<const uint32_t *>(ws + ws_off[j].second);
+            PrepItem &q = pp.item[pp.n_items++];
+            q.x = it.x;
+            q.norm_w = it.norm_w;
+            q.sw = kSW;
+            q.head = kFmt == kFmtI8 ? 1 : 0;
+            q.b = ws + ws_off[j].first;
+            q.meta = reinterpret_cast<uint32_t *>(ws + ws_off[j].second);
+            q.k = it.k;
+            q.m = it.m;
+            q.stages = it.stages;
+            q.cstages = it.cstages;
+            q.task0 = pp.n_tasks;
+            if (it.cstages * kSW > kPrepWords * kPrepThreads) return TERN_ERR_SHAPE;  // cannot happen: m >= 2
+            pp.n_tasks += (it.stages + it.cstages - 1) / it.cstages * it.m;
+        }
+        cudaLaunchConfig_t pcfg = {};
+        pcfg.gridDim = dim3((unsigned)pp.n_tasks, 1, 1);
+        pcfg.blockDim = dim3(kPrepThreads, 1, 1);
+        pcfg.stream = stream;
+        cudaLaunchAttribute pattr;
+        pattr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        pattr.val.programmaticStreamSerializationAllowed = 1;
+        pcfg.attrs = &pattr;
+        pcfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&pcfg, k_tern_bprep, pp) != cudaSuccess) return TERN_ERR_CUDA;
+    }
+    // contiguous runs of units with balanced stage counts
+    const int ctas = units < sms ? units : (sms < kMaxCtas ? sms : kMaxCtas);
+    long long total = 0;
+    for (long long c : unit_cost) total += c;
+    int u = 0;
+    long long acc = 0;
+    prm.unit_start[0] = 0;
+    for (int b = 1; b < ctas; ++b) {
+        const long long target = total * b / ctas;
+        while (u < units && acc + unit_cost[u] / 2 < target) acc += unit_cost[u++];
+        prm.unit_start[b] = u;
+    }
+    prm.unit_start[ctas] = units;
+    for (int b = 0, j = 0; b < ctas; ++b) {
+        while (j + 1 < cnt && prm.item[j + 1].unit0 <= prm.unit_start[b]) ++j;
+        prm.item_start[b] = j;
+    }
+    for (int b = 0; b < ctas; ++b) {
+        long long st = 0;
+        for (int q = prm.unit_start[b]; q < prm.unit_start[b + 1]; ++q) st += unit_cost[q];
+        prm.stages_cta[b] = (int)st;
+    }
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)ctas, 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, k_tern_batched<kFmt>, prm, maps) != cudaSuccess) return TERN_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return TERN_ERR_CUDA;
+    return TERN_OK;
+}
+
+// Launches the batch, group by group.  fixed_ws: see launch_group.  norm_w:
+// nullptr, or per item the RMSNorm channel weights (nullptr for an item
+// without a norm), with eps.
+tern_status run_batched(const tern_batch_item *items, int n, cudaStream_t stream, unsigned char *fixed_ws,
+                        const float *const *norm_w = nullptr, float eps = 0.f)
+{
     int begin = 0;
+    std::vector<Job> jobs;
     for (const int end : plan_groups(items, n)) {
-        Params prm;
-        std::memset(&prm, 0, sizeof(prm));
-        Maps maps;
-        std::memset(&maps, 0, sizeof(maps));
-        std::vector<long long> unit_cost;
-        int cnt = 0, units = 0, n_maps = 0;
+        jobs.clear();
         for (int idx = begin; idx < end; ++idx) {
             const tern_batch_item &b = items[idx];
             if (b.w->rows == 0) continue;
@@ -1119,120 +1507,40 @@ tern_status run_batched(const tern_batch_item *items, int n, cudaStream_t stream
                 if (st != TERN_OK) return st;
                 continue;
             }
-            Item &it = prm.item[cnt];
-            it.scale_g = b.w->scale;
-            it.scale_u = b.up ? b.up->scale : nullptr;
-            it.x = b.x;
-            it.y = b.y;
-            it.rows = b.w->rows;
-            it.k = b.w->k;
-            it.m = b.m;
-            it.swiglu = b.up != nullptr;
-            it.norm_w = norm_w != nullptr ? norm_w[idx] : nullptr;
-            chunk_plan(it.k, it.m, it.stages, it.cstages);
-            it.unit0 = units;
-            it.map = n_maps;
-            const int tile_rows = it.swiglu ? 64 : 128;
-            const int tiles = (it.rows + tile_rows - 1) / tile_rows;
-            if (!make_code_map(&maps.m[n_maps++], b.w->codes, it.rows, it.k / 16, tile_rows)) return TERN_ERR_CUDA;
-            if (it.swiglu && !make_code_map(&maps.m[n_maps++], b.up->codes, it.rows, it.k / 16, tile_rows))
-                return TERN_ERR_CUDA;
-            for (int t = 0; t < tiles; ++t) unit_cost.push_back(it.stages);
-            units += tiles;
-            ++cnt;
+            Job jb;
+            jb.codes_g = b.w->codes;
+            jb.codes_u = b.up ? b.up->codes : nullptr;
+            jb.scale_g = b.w->scale;
+            jb.scale_u = b.up ? b.up->scale : nullptr;
+            jb.x = b.x;
+            jb.y = b.y;
+            jb.norm_w = norm_w != nullptr ? norm_w[idx] : nullptr;
+            jb.rows = b.w->rows;
+            jb.k = b.w->k;
+            jb.m = b.m;
+            jb.kw = b.w->k / 16;
+            jobs.push_back(jb);
         }
         begin = end;
-        if (cnt == 0) continue;
-        prm.n_items = cnt;
-        prm.eps = eps;
-        prm.wait_limit = wait_limit();
-
-        // Items with m >= 2 take their B from the workspace, written by one
-        // k_tern_bprep launch just before (one CTA per item, K chunk and
-        // activation row): per item the padded K's one-band words (1024m
-        // bytes per stage), then kMetaWords of metadata per chunk.  Items
-        // with m = 1 are built by the persistent kernel's staging warps.
-        PrepParams pp;
-        std::memset(&pp, 0, sizeof(pp));
-        pp.eps = eps;
-        size_t ws_need = 0;
-        std::vector<std::pair<size_t, size_t>> ws_off(cnt);
-        for (int j = 0; j < cnt; ++j) {
-            const Item &it = prm.item[j];
-            if (it.m < 2) continue;
-            ws_off[j].first = ws_need;
-            ws_off[j].second = ws_need + prep_b_bytes(it.stages, it.m);
-            ws_need += prep_bytes(it.stages, it.cstages, it.m);
-        }
-        if (ws_need > 0) {
-            unsigned char *ws = fixed_ws != nullptr ? fixed_ws : static_cast<unsigned char *>(workspace(stream, ws_need));
-            if (ws == nullptr) return TERN_ERR_CUDA;
-            for (int j = 0; j < cnt; ++j) {
-                Item &it = prm.item[j];
-                if (it.m < 2) continue;
-                it.bsrc = ws + ws_off[j].first;
-                it.meta = reinterpret_cast<const uint32_t *>(ws + ws_off[j].second);
-                PrepItem &q = pp.item[pp.n_items++];
-                q.x = it.x;
-                q.norm_w = it.norm_w;
-                q.b = ws + ws_off[j].first;
-                q.meta = reinterpret_cast<uint32_t *>(ws + ws_off[j].second);
-                q.k = it.k;
-                q.m = it.m;
-                q.stages = it.stages;
-                q.cstages = it.cstages;
-                q.task0 = pp.n_tasks;
-                if (it.cstages * kStageWords > kPrepWords * kPrepThreads) return TERN_ERR_SHAPE;  // cannot happen: m >= 2
-                pp.n_tasks += (it.stages + it.cstages - 1) / it.cstages * it.m;
-            }
-            cudaLaunchConfig_t pcfg = {};
-            pcfg.gridDim = dim3((unsigned)pp.n_tasks, 1, 1);
-            pcfg.blockDim = dim3(kPrepThreads, 1, 1);
-            pcfg.stream = stream;
-            cudaLaunchAttribute pattr;
-            pattr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-            pattr.val.programmaticStreamSerializationAllowed = 1;
-            pcfg.attrs = &pattr;
-            pcfg.numAttrs = 1;
-            if (cudaLaunchKernelEx(&pcfg, k_tern_bprep, pp) != cudaSuccess) return TERN_ERR_CUDA;
-        }
-        // contiguous runs of units with balanced stage counts
-        const int ctas = units < sms ? units : (sms < kMaxCtas ? sms : kMaxCtas);
-        long long total = 0;
-        for (long long c : unit_cost) total += c;
-        int u = 0;
-        long long acc = 0;
-        prm.unit_start[0] = 0;
-        for (int b = 1; b < ctas; ++b) {
-            const long long target = total * b / ctas;
-            while (u < units && acc + unit_cost[u] / 2 < target) acc += unit_cost[u++];
-            prm.unit_start[b] = u;
-        }
-        prm.unit_start[ctas] = units;
-        for (int b = 0, j = 0; b < ctas; ++b) {
-            while (j + 1 < cnt && prm.item[j + 1].unit0 <= prm.unit_start[b]) ++j;
-            prm.item_start[b] = j;
-        }
-        for (int b = 0; b < ctas; ++b) {
-            long long st = 0;
-            for (int q = prm.unit_start[b]; q < prm.unit_start[b + 1]; ++q) st += unit_cost[q];
-            prm.stages_cta[b] = (int)st;
-        }
-
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)ctas, 1, 1);
-        cfg.blockDim = dim3(kThreads, 1, 1);
-        cfg.dynamicSmemBytes = kSmemBytes;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr;
-        attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr.val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, k_tern_batched, prm, maps) != cudaSuccess) return TERN_ERR_CUDA;
-        if (cudaGetLastError() != cudaSuccess) return TERN_ERR_CUDA;
+        if (jobs.empty()) continue;
+        const tern_status st = launch_group<kFmtTern>(jobs.data(), (int)jobs.size(), stream, fixed_ws, eps, nullptr);
+        if (st != TERN_OK) return st;
     }
     return TERN_OK;
+}
+
+// The int8 head's argmax keys start below every real key (a real key's top
+// half is the order-preserving image of a finite logit, never zero).
+__global__ void k_head_keys_init(unsigned long long *keys)
+{
+    if (threadIdx.x < 8) keys[threadIdx.x] = 0ull;
+}
+
+// The int8 head's argmax: the key of each activation row back to its row.
+__global__ void k_head_argmax_finish(const unsigned long long *keys, int32_t *argmax, int m)
+{
+    const int q = (int)threadIdx.x;
+    if (q < m) argmax[q] = (int32_t)(~(uint32_t)(keys[q] & 0xFFFFFFFFull));
 }
 
 }  // namespace
@@ -1246,6 +1554,31 @@ tern_status gemm_batched_rmsnorm(const tern_batch_item *items, const float *cons
                                  cudaStream_t stream)
 {
     return run_batched(items, n, stream, nullptr, norm_w, eps);
+}
+
+tern_status head_argmax(const tern_i8_matrix *w, const uint16_t *x, int m, const float *norm_w, float eps,
+                        float *logits, int32_t *argmax, cudaStream_t stream)
+{
+    unsigned long long *keys = static_cast<unsigned long long *>(workspace(stream, 8 * sizeof(unsigned long long), 1));
+    if (keys == nullptr) return TERN_ERR_CUDA;
+    Job jb;
+    jb.codes_g = reinterpret_cast<const uint32_t *>(w->w);
+    jb.codes_u = nullptr;
+    jb.scale_g = w->scale;
+    jb.scale_u = nullptr;
+    jb.x = x;
+    jb.y = logits;
+    jb.norm_w = norm_w;
+    jb.rows = w->rows;
+    jb.k = w->k;
+    jb.m = m;
+    jb.kw = w->k / 4;
+    k_head_keys_init<<<1, 32, 0, stream>>>(keys);
+    if (cudaGetLastError() != cudaSuccess) return TERN_ERR_CUDA;
+    const tern_status st = launch_group<kFmtI8>(&jb, 1, stream, nullptr, eps, keys);
+    if (st != TERN_OK) return st;
+    k_head_argmax_finish<<<1, 32, 0, stream>>>(keys, argmax, m);
+    return cudaGetLastError() == cudaSuccess ? TERN_OK : TERN_ERR_CUDA;
 }
 
 tern_status gemm_batched_noalloc(const tern_batch_item *items, int n, cudaStream_t stream)

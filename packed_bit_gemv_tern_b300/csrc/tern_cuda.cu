@@ -239,6 +239,22 @@ extern "C" tern_status tern_gemm_batched_rmsnorm(const tern_batch_item *items, c
     return gemm_batched_rmsnorm(items, norm_w, eps, n, (cudaStream_t)stream);
 }
 
+extern "C" tern_status tern_lmhead_argmax(const tern_i8_matrix *w, const uint16_t *x, int32_t m, const float *norm_w,
+                                          float eps, float *logits, int32_t *argmax, void *stream)
+{
+    if (w == nullptr || w->w == nullptr || w->scale == nullptr || x == nullptr || logits == nullptr ||
+        argmax == nullptr)
+        return TERN_ERR_NULL;
+    if (w->rows < 1 || w->k < 64 || w->k % 64 != 0) return TERN_ERR_SHAPE;
+    if (m < 1 || m > TERN_MAX_M) return TERN_ERR_M_RANGE;
+    if ((int64_t)m * w->k * 2 > TERN_MAX_X_BYTES) return TERN_ERR_SHAPE;
+    if (!aligned(w->w, 16) || !aligned(w->scale, 4) || !aligned(x, 16) || !aligned(logits, 4) || !aligned(argmax, 4) ||
+        (norm_w != nullptr && !aligned(norm_w, 16)))
+        return TERN_ERR_ALIGN;
+    if (!(eps >= 0.f && eps <= 3.4e38f)) return TERN_ERR_VALUE;
+    return head_argmax(w, x, m, norm_w, eps, logits, argmax, (cudaStream_t)stream);
+}
+
 extern "C" tern_status tern_gemm_batched_noalloc(const tern_batch_item *items, int32_t n, void *stream)
 {
     const tern_status st = check_batch(items, n);

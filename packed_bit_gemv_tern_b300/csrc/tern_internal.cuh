@@ -32,6 +32,9 @@ tern_status take_mma_error();
 // Number of kernel launches gemm_batched makes for these items (host only).
 int batched_launches(const tern_batch_item *items, int n);
 tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t s);
+// int8 head logits and per-row argmax (arguments checked by the caller).
+tern_status head_argmax(const tern_i8_matrix *w, const uint16_t *x, int m, const float *norm_w, float eps,
+                        float *logits, int32_t *argmax, cudaStream_t s);
 // As gemm_batched, each item with norm_w[i] != nullptr normalised first (RMSNorm).
 tern_status gemm_batched_rmsnorm(const tern_batch_item *items, const float *const *norm_w, float eps, int n,
                                  cudaStream_t s);

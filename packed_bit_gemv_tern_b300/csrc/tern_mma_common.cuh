@@ -248,6 +248,13 @@ __device__ __forceinline__ uint4 transpose_row(const uint32_t (&p)[8])
                       __byte_perm(p13, p57, 0x7531));
 }
 
+// Eight pairs of split bytes -> one 16-byte B row in plain k order (the
+// int8 head's weights are decoded in k order).
+__device__ __forceinline__ uint4 natural_row(const uint32_t (&p)[8])
+{
+    return make_uint4(p[0] | (p[1] << 16), p[2] | (p[3] << 16), p[4] | (p[5] << 16), p[6] | (p[7] << 16));
+}
+
 // RMSNorm prologue (model page spec table: RMSNorm, eps 1e-6, ahead of the
 // q/k/v and gate/up projections).  Per activation row the mean square is
 // taken in fp64 (every bf16 square is exact there), the row factor
@@ -266,6 +273,17 @@ __device__ __forceinline__ double sumsq16(const uint4 a, const uint4 b)
         s = fma(lo, lo, s);
         s = fma(hi, hi, s);
     }
+    return s;
+}
+
+// Sum of the 16 bf16 activations of one word, in fp64.
+__device__ __forceinline__ double sum16(const uint4 a, const uint4 b)
+{
+    const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    double s = 0.0;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        s += (double)__uint_as_float(v[j] << 16) + (double)__uint_as_float(v[j] & 0xFFFF0000u);
     return s;
 }
 
@@ -294,15 +312,21 @@ __device__ __forceinline__ void rmsnorm_word(uint4 &a, uint4 &b, const float4 *g
 }
 
 // One word (16 k) of one activation row -> its two one-band B rows: out[0]
-// = hi, out[1] = lo, at scale sc = 2^s (split_pair).
-__device__ __forceinline__ void split_word1(const uint4 a, const uint4 b, float sc, uint4 (&out)[2])
+// = hi, out[1] = lo, at scale sc = 2^s (split_pair); in the ternary decode's
+// column order, or in k order when nat (the int8 head).
+__device__ __forceinline__ void split_word1(const uint4 a, const uint4 b, float sc, uint4 (&out)[2], bool nat = false)
 {
     const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     uint32_t h[8], l[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) split_pair(v[q], sc, h[q], l[q]);
-    out[0] = transpose_row(h);
-    out[1] = transpose_row(l);
+    if (nat) {
+        out[0] = natural_row(h);
+        out[1] = natural_row(l);
+    } else {
+        out[0] = transpose_row(h);
+        out[1] = transpose_row(l);
+    }
 }
 
 // One word (16 k) of one activation row -> its four B rows: out[0], out[1]
@@ -314,7 +338,7 @@ __device__ __forceinline__ void split_word1(const uint4 a, const uint4 b, float 
 // A is exact by construction and band B is exact down to 2^-13 of its own
 // maximum.
 __device__ __forceinline__ void split_word2(const uint4 a, const uint4 b, float scA, float scB, uint32_t tb2,
-                                            uint4 (&out)[4])
+                                            uint4 (&out)[4], bool nat = false)
 {
     const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
     uint32_t ha[8], la[8], hb[8], lb[8];
@@ -324,10 +348,17 @@ __device__ __forceinline__ void split_word2(const uint4 a, const uint4 b, float 
         split_pair(v[q] & in_a, scA, ha[q], la[q]);
         split_pair(v[q] & ~in_a, scB, hb[q], lb[q]);
     }
-    out[0] = transpose_row(ha);
-    out[1] = transpose_row(la);
-    out[2] = transpose_row(hb);
-    out[3] = transpose_row(lb);
+    if (nat) {
+        out[0] = natural_row(ha);
+        out[1] = natural_row(la);
+        out[2] = natural_row(hb);
+        out[3] = natural_row(lb);
+    } else {
+        out[0] = transpose_row(ha);
+        out[1] = transpose_row(la);
+        out[2] = transpose_row(hb);
+        out[3] = transpose_row(lb);
+    }
 }
 
 // Eight packed words (128 codes of one row) -> 32 registers of e4m3 bytes:

@@ -175,6 +175,24 @@ def test_device_entry_points_reject_before_launch(lib):
     arr[1].m = 9  # a bad item is reported before the norm arguments
     assert f(pa, None, ctypes.c_float(-1.0), 2, None) == tern.TERN_ERR_M_RANGE
     arr[1].m = 1
+    # int8 head: every argument is checked before a launch
+    h = tern.CI8Matrix(10, 128, 0x7000, 0x7100)
+    lg, am = ctypes.c_void_p(0x8000), ctypes.c_void_p(0x9000)
+    f = lib.tern_lmhead_argmax
+    e6 = ctypes.c_float(1e-6)
+    assert f(None, x, 1, None, e6, lg, am, None) == tern.TERN_ERR_NULL
+    assert f(ref(h), None, 1, None, e6, lg, am, None) == tern.TERN_ERR_NULL
+    assert f(ref(h), x, 1, None, e6, lg, None, None) == tern.TERN_ERR_NULL
+    assert f(ref(tern.CI8Matrix(0, 128, 0x7000, 0x7100)), x, 1, None, e6, lg, am, None) == tern.TERN_ERR_SHAPE
+    assert f(ref(tern.CI8Matrix(10, 96, 0x7000, 0x7100)), x, 1, None, e6, lg, am, None) == tern.TERN_ERR_SHAPE
+    assert f(ref(tern.CI8Matrix(10, 24576, 0x7000, 0x7100)), x, 8, None, e6, lg, am, None) == tern.TERN_ERR_SHAPE
+    for m in (0, 9):
+        assert f(ref(h), x, m, None, e6, lg, am, None) == tern.TERN_ERR_M_RANGE
+    assert f(ref(tern.CI8Matrix(10, 128, 0x7008, 0x7100)), x, 1, None, e6, lg, am, None) == tern.TERN_ERR_ALIGN
+    assert f(ref(h), ctypes.c_void_p(0x3008), 1, None, e6, lg, am, None) == tern.TERN_ERR_ALIGN
+    assert f(ref(h), x, 1, ctypes.c_void_p(0x6004), e6, lg, am, None) == tern.TERN_ERR_ALIGN
+    assert f(ref(h), x, 1, None, e6, lg, ctypes.c_void_p(0x9002), None) == tern.TERN_ERR_ALIGN
+    assert f(ref(h), x, 1, None, ctypes.c_float(-1.0), lg, am, None) == tern.TERN_ERR_VALUE
     # empty problems succeed without a launch, with NULL pointers
     empty = tern.CMatrix(0, 64, None, None, None)
     assert lib.tern_gemv(ref(empty), None, None, None) == tern.TERN_OK
