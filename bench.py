@@ -51,6 +51,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--rotate-mb", type=int, default=400,
                     help="c0-c3: MiB of distinct packed weights one step streams (keep above the 126 MB L2)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the single-call, ordered-sweep and output-head measurements")
     ap.add_argument("--api", default="batched", choices=["batched", "single"],
                     help="batched: one persistent tern_gemm_batched launch per step; single: one launch per call")
     return ap.parse_args()
@@ -211,6 +213,86 @@ def spread_stats(us_per_call) -> dict:
 
     return {"steps": len(per), "us_per_call_p10": pct(0.1), "us_per_call_median": pct(0.5),
             "us_per_call_p90": pct(0.9)}
+
+
+def _graph_ms(fn, stream, reps: int, warm: int = 3) -> float:
+    """Mean ms of one replay of a CUDA graph of fn(), after an eager pass and
+    warm-up replays, between CUDA events on the launching stream."""
+    import torch
+    with torch.cuda.stream(stream):
+        fn()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            g.replay()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    e1.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def extras(args, dev, stream, wl, peak):
+    """Three more measurements on rank 0, each never failing the bench line:
+    single_call (c1 as back-to-back tern_gemv launches in one graph, one
+    launch per call), ordered_sweep (the 36-layer decode sweep as 4 launch
+    groups per layer in dependency order, 144 tern_gemm_batched calls per
+    token) and lm_head (the 151,936 x 4,096 int8 output head with the fused
+    argmax, m = 1)."""
+    import torch
+
+    import packed_bit_gemv_tern_b300 as tern
+    from packed_bit_gemv_tern_b300 import synth, workloads
+    out = {}
+    try:
+        wl1 = wl if args.workload == "c1" else workloads.build("c1", device=dev, rotate_bytes=400 * workloads.MiB)
+        ms = _graph_ms(lambda: workloads.run_calls(wl1.calls, stream), stream, reps=100)
+        n = len(wl1.calls)
+        ach = wl1.algorithmic_bytes / (ms * 1e-3) / 1e9
+        out["single_call"] = {"workload": f"c1 as {n} back-to-back tern_gemv launches per graph replay",
+                              "us_per_call": round(1e3 * ms / n, 3), "gbs": round(ach, 2), "frac": round(ach / peak, 4)}
+    except Exception as e:
+        out["single_call"] = {"error": f"{type(e).__name__}: {e}"}
+    try:
+        groups, packed, keep = workloads.layer_sweep(dev)
+        ms = _graph_ms(lambda: [tern.tern_gemm_batched(g, stream) for g in groups], stream, reps=20)
+        gbs = packed / (ms * 1e-3) / 1e9
+        out["ordered_sweep"] = {"workload": f"{synth.LAYERS} layers x (q|k|v, o, gate/up SwiGLU, down) in order, "
+                                            "4 layers of distinct weights reused cyclically (184 MB)",
+                                "groups_per_token": len(groups), "us_per_token": round(1e3 * ms, 2),
+                                "gbs_packed": round(gbs, 2), "frac": round(gbs / peak, 4)}
+        del keep
+    except Exception as e:
+        out["ordered_sweep"] = {"error": f"{type(e).__name__}: {e}"}
+    head = None
+    try:
+        rng = np.random.default_rng(777)
+        rows, k = 151936, 4096
+        w = rng.integers(-128, 128, (rows, k), dtype=np.int8)
+        sc = rng.uniform(0.5e-3, 2e-3, rows).astype(np.float32)
+        dw = tern.I8Matrix.from_host(w, sc, device=dev)
+        del w
+        xb = synth.activations(rng, 1, k)
+        x = torch.from_numpy(xb.view(np.int16)).to(dev).view(torch.bfloat16)
+        logits = torch.empty((1, rows), dtype=torch.float32, device=dev)
+        am = torch.empty((1,), dtype=torch.int32, device=dev)
+        ms = _graph_ms(lambda: tern.tern_lmhead_argmax(dw, x, 1, logits, am, stream=stream), stream, reps=50)
+        alg = rows * k + 8 * rows + 2 * k  # int8 weights, scales, logits, x
+        ach = alg / (ms * 1e-3) / 1e9
+        consistent = int(am.item()) == int(torch.argmax(logits[0]).item())
+        head = {"workload": "int8 output head 151,936 x 4,096 (622 MB) + per-row scale, m = 1, fused argmax",
+                "us_per_call": round(1e3 * ms, 2), "gbs": round(ach, 2), "frac": round(ach / peak, 4),
+                "launches_per_call": 3, "argmax_matches_logits": consistent}
+    except Exception as e:
+        head = {"error": f"{type(e).__name__}: {e}"}
+    return out, head
 
 
 def persistent_launches(batch) -> int:
@@ -426,11 +508,20 @@ def run_ours(args, dist: Dist):
     if not args.no_e2e:
         e2e = run_e2e(args, wl, stream, dist, batch)
 
+    more, head = ({}, None)
+    if dist.rank == 0 and not args.no_extras:
+        more, head = extras(args, dev, stream, wl, peak)
+
     cpu = None
     if dist.rank == 0 and not args.no_cpu_baseline:
+        # median of three samples on every host core, and one on a single core
         threads = os.cpu_count() or 1
-        gbs, b, dt, desc = oracle_sample_rate(wl, max(1.0, 12.0 / threads), threads)
-        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle", "sample": desc}
+        runs = [oracle_sample_rate(wl, max(1.0, 4.0 / threads), threads) for _ in range(3)]
+        gbs = statistics.median(r[0] for r in runs)
+        one = oracle_sample_rate(wl, 3.0, 1)
+        cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": runs[0][3], "runs": [round(r[0], 4) for r in runs], "stat": "median of 3",
+               "value_1core": round(one[0], 4), "sample_1core": one[3]}
 
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": dist.world,
@@ -443,6 +534,7 @@ def run_ours(args, dist: Dist):
                    "l2": "inputs larger than L2: each step streams %.0f MB of distinct buffers" % (packed / 1e6),
                    "graph": "one CUDA graph per step, replayed", "parallelism": f"replicas x{dist.world}",
                    "gpu": torch.cuda.get_device_name(dev), "spread": spread,
+                   "single_call": more.get("single_call"), "ordered_sweep": more.get("ordered_sweep"),
                    "api": (f"tern_gemm_batched: {main_launches} persistent launch(es) per step"
                            + (f" and {prep_launches} activation-preparing launch(es)" if prep_launches else "")
                            if args.api == "batched" else "one tern_* launch per call")},
@@ -454,6 +546,7 @@ def run_ours(args, dist: Dist):
                      "duration": ("CUDA-event step time / persistent launches per step"
                                   + (" (includes the activation-preparing launch)" if prep_launches else ""))},
         "clocks": clk,
+        "lm_head": head,
         "gpu_launches": args.steps * launches_per_step,
         "e2e": e2e,
         "cpu_baseline": cpu,

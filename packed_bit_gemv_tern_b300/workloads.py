@@ -239,3 +239,38 @@ def io_copy(wl: Workload):
 
 def _clone(w: TernMatrix) -> TernMatrix:
     return TernMatrix(w.codes.clone(), w.scale.clone(), w.k, None if w.rowsum is None else w.rowsum.clone())
+
+
+def layer_sweep(device="cuda", layers: int | None = None, distinct_layers: int = 4, seed: int = 4242):
+    """The decode sweep in dependency order: per layer four launch groups,
+    q|k|v, o, the gate/up pair (fused SwiGLU) and down, each one
+    tern_gemm_batched call, so a token is 4 * layers launch groups in stream
+    order.  ``distinct_layers`` layers of weights (about 46 MB each, more than
+    the 126 MB L2 together) are drawn and reused cyclically over the layers.
+    Returns (groups, packed_bytes_per_token, buffers): groups is the list of
+    item arrays in call order; buffers keeps every tensor alive."""
+    nl = synth.LAYERS if layers is None else layers
+    rng = np.random.default_rng(seed)
+    shapes = dict((n, (r, k)) for n, r, k in synth.LAYER_LINEARS)
+    mats = []
+    for _ in range(distinct_layers):
+        d = {}
+        for name, (rows, k) in shapes.items():
+            d[name] = device_matrix(synth.linear(rng, rows, k, name=name), device)
+        mats.append(d)
+    groups, buffers, packed = [], [], 0
+    for layer in range(nl):
+        d = mats[layer % distinct_layers]
+        plan = [[("q", None), ("k", None), ("v", None)], [("o", None)], [("gate", "up")], [("down", None)]]
+        for grp in plan:
+            items = []
+            for name, up in grp:
+                w = d[name]
+                x, _ = _x(rng, 1, w.k, device)
+                y = _y(1, w.rows, device)
+                items.append((w, d[up] if up else None, x, y, 1))
+                buffers += [x, y]
+                packed += w.packed_bytes + (d[up].packed_bytes if up else 0)
+            groups.append(batch_items(items))
+    buffers.append(mats)
+    return groups, packed, buffers
