@@ -44,7 +44,8 @@ def parse():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=100)
-    ap.add_argument("--workload", default="c1", choices=["c0", "c1", "c2", "c3", "c4"])
+    ap.add_argument("--workload", default="c1", choices=["c0", "c1", "c2", "c3", "c4", "head"],
+                    help="head: the int8 output head alone (151,936 x 4,096, m = 1, fused argmax)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -427,6 +428,77 @@ def _host_only_workload(name):
     return wl
 
 
+def run_head(args, dist: Dist):
+    """--workload head: the int8 output head with the fused argmax as the
+    timed step (one tern_lmhead_argmax call; 622 MB of weights, more than the
+    L2), the same timing protocol as the ternary workloads."""
+    import torch
+
+    import packed_bit_gemv_tern_b300 as tern
+    from packed_bit_gemv_tern_b300 import synth
+    dev = torch.device("cuda", dist.local)
+    torch.cuda.set_device(dev)
+    tern.load()
+    stream = torch.cuda.Stream(device=dev)
+    rng = np.random.default_rng(777 + 1000 * dist.rank)
+    rows, k = 151936, 4096
+    w = rng.integers(-128, 128, (rows, k), dtype=np.int8)
+    sc = rng.uniform(0.5e-3, 2e-3, rows).astype(np.float32)
+    dw = tern.I8Matrix.from_host(w, sc, device=dev)
+    del w
+    x = torch.from_numpy(synth.activations(rng, 1, k).view(np.int16)).to(dev).view(torch.bfloat16)
+    logits = torch.empty((1, rows), dtype=torch.float32, device=dev)
+    am = torch.empty((1,), dtype=torch.int32, device=dev)
+    with torch.cuda.stream(stream):
+        tern.tern_lmhead_argmax(dw, x, 1, logits, am, stream=stream)
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        tern.tern_lmhead_argmax(dw, x, 1, logits, am, stream=stream)
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    stream.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        ev1.record(stream)
+    ev1.synchronize()
+    dist.barrier()
+    clk = clocks.stop()
+    ms = dist.max(ev0.elapsed_time(ev1))
+    if tern.tern_last_device_error(stream) != tern.TERN_OK:
+        raise SystemExit("device error during the timed region")
+    step_ms = ms / args.steps
+    alg = rows * k + 8 * rows + 2 * k
+    ach = alg / (step_ms * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    line = {
+        "metric": "int8 output-head GB/s and µs/call at M=1 (fraction of B300 HBM peak)",
+        "value": round(dist.world * rows * k / (step_ms * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 6), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 x, int8 w, fp32 acc", "data": "synthetic (seeded)",
+        "config": {"workload": "head: int8 output head 151,936 x 4,096 + per-row scale, m = 1, fused argmax",
+                   "us_per_call": round(1e3 * step_ms, 3), "graph": "one CUDA graph per call, replayed",
+                   "l2": "622 MB of weights per call, more than the L2",
+                   "argmax_matches_logits": int(am.item()) == int(torch.argmax(logits[0]).item())},
+        "roofline": {"bound": "hbm", "achieved": round(ach, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(ach / peak, 4), "peak_kind": peak_kind, "traffic": None,
+                     "bytes_per_launch": alg, "duration": "CUDA-event time per call (3 launches, the head kernel dominant)"},
+        "clocks": clk, "gpu_launches": 3 * args.steps, "e2e": None, "cpu_baseline": None,
+    }
+    if dist.rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 def run_ours(args, dist: Dist):
     import torch
 
@@ -666,7 +738,12 @@ def main():
     dist = Dist()
     try:
         if args.impl == "reference":
+            if args.workload == "head":
+                print(json.dumps({"impl": "reference", "unavailable": "no oracle arm for the head workload"}))
+                return 0
             return run_reference(args, dist)
+        if args.workload == "head":
+            return run_head(args, dist)
         return run_ours(args, dist)
     finally:
         dist.close()

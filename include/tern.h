@@ -40,18 +40,21 @@
  * channels), the chunk is taken in two bands instead: band A holds the
  * elements within 2^13 of the maximum, band B the others under a scale of
  * their own (2^f <= band-B max < 2^(f+1)), exact down to 2^-13 of it and
- * off by at most 2^(f-21) below.  Within a band the sums are fp32; bands,
- * chunks and split-K ranks are added as exact fp32 pairs (TwoSum) and
- * rounded once.
+ * off by at most 2^(f-21) below.  Within a band the sums are fp32; bands
+ * and split-K ranks are added as exact fp32 pairs (TwoSum) and rounded
+ * once.  The batched kernel adds a unit's chunks in plain fp32 while every
+ * chunk so far has had one band (each is then within 2^-24 of its own
+ * sum|x|), and as pairs from the unit's first two-band chunk on.
  *
  * Conventions for every entry point:
  *   - The caller owns every buffer it passes.  Device memory the library
  *     holds itself: one error word per kernel family and the
  *     TERN_NOALLOC_WS_BYTES array of tern_gemm_batched_noalloc (both
  *     module-scope, set up when the library's kernels are loaded on a
- *     device), and the workspace tern_gemm_batched allocates on first need
- *     (see there).  tern_gemv, tern_gemv_swiglu, tern_gemm_smallm*,
- *     tern_unpack and tern_gemm_batched_noalloc never allocate.
+ *     device), and the workspaces tern_gemm_batched (and _rmsnorm) and
+ *     tern_lmhead_argmax allocate on first need (see there).  tern_gemv,
+ *     tern_gemv_swiglu, tern_gemm_smallm*, tern_unpack and
+ *     tern_gemm_batched_noalloc never allocate.
  *   - Encoded TMA descriptors of weight matrices are cached on the host by
  *     (codes pointer, shape); a descriptor holds only that address and
  *     shape, so a later matrix at the same address with the same shape
