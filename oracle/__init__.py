@@ -63,8 +63,12 @@ def _load():
             lib.orc_rmsnorm_gemm.argtypes = [p, p, i64, i64, p, p, ctypes.c_double, i64, p, p, i64, i64]
             lib.orc_i8_gemm.argtypes = [p, p, i64, i64, p, i64, p, p, i64, i64]
             lib.orc_argmax.argtypes = [p, i64, i64, p]
+            lib.orc_pack5.argtypes = [p, i64, i64, p]
+            lib.orc_unpack5.argtypes = [p, i64, i64, p]
+            lib.orc_gemm5.argtypes = [p, p, i64, i64, p, i64, p, i64, i64]
             for f in (lib.orc_pack, lib.orc_unpack, lib.orc_stats, lib.orc_gemm, lib.orc_swiglu, lib.orc_rmsnorm,
-                      lib.orc_rmsnorm_gemm, lib.orc_i8_gemm, lib.orc_argmax):
+                      lib.orc_rmsnorm_gemm, lib.orc_i8_gemm, lib.orc_argmax, lib.orc_pack5, lib.orc_unpack5,
+                      lib.orc_gemm5):
                 f.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -258,3 +262,35 @@ def argmax(y: np.ndarray) -> np.ndarray:
     idx = np.zeros(m, dtype=np.int64)
     _check(_load().orc_argmax(_ptr(y), m, rows, _ptr(idx)), "argmax")
     return idx
+
+
+def pack5(t: np.ndarray) -> np.ndarray:
+    """int8 [rows, k] (k % 80 == 0) -> uint8 [rows, k//5] in the base-3 format."""
+    t = np.ascontiguousarray(t, dtype=np.int8)
+    rows, k = t.shape
+    codes = np.zeros((rows, k // 5), dtype=np.uint8)
+    _check(_load().orc_pack5(_ptr(t), rows, k, _ptr(codes)), "pack5")
+    return codes
+
+
+def unpack5(codes: np.ndarray, k: int) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    rows = codes.shape[0]
+    t = np.zeros((rows, k), dtype=np.int8)
+    _check(_load().orc_unpack5(_ptr(codes), rows, k, _ptr(t)), "unpack5")
+    return t
+
+
+def gemm5(codes: np.ndarray, scale: np.ndarray, k: int, x_bits: np.ndarray, threads: int = 1,
+          rows_subset=None) -> np.ndarray:
+    """y [m, rows] float64 = scale * (T @ x) from base-3 codes."""
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scale = np.ascontiguousarray(scale, dtype=np.float32)
+    x_bits = np.ascontiguousarray(np.atleast_2d(x_bits), dtype=np.uint16)
+    rows = codes.shape[0]
+    m = x_bits.shape[0]
+    y = np.zeros((m, rows), dtype=np.float64)
+    lib = _load()
+    _run_rows(lambda b, e: lib.orc_gemm5(_ptr(codes), _ptr(scale), rows, k, _ptr(x_bits), m, _ptr(y), b, e),
+              rows, threads, rows_subset)
+    return y

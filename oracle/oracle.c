@@ -292,3 +292,69 @@ int orc_argmax(const double *y, int64_t m, int64_t rows, int64_t *idx)
     }
     return ORC_OK;
 }
+
+/*
+ * Denser packing (Neutrino-1 8B model page, "Where the bytes live" and the
+ * "three doors" of the format discussion: the shipped lane spends more bits
+ * per weight than a ternary value needs; SURVEY's next rows name base-3
+ * packing).  This project's base-3 format, defined here and nowhere on the
+ * pages:
+ *   - a row of K weights (K a multiple of 80, padded with zero weights) is
+ *     K/5 bytes; byte j holds weights 5j .. 5j+4;
+ *   - byte value b = sum_{i<5} (t[5j+i] + 1) * 3^i  (least significant digit
+ *     first), so b is in [0, 242]; bytes 243..255 are invalid;
+ *   - 1.6 bits per weight against 2 for the 2-bit format.
+ */
+int orc_pack5(const int8_t *t, int64_t rows, int64_t k, uint8_t *codes)
+{
+    if (rows < 0 || k < 0 || k % 80 != 0) return ORC_BAD_SHAPE;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t j = 0; j < k / 5; ++j) {
+            unsigned b = 0, p = 1;
+            for (int i = 0; i < 5; ++i) {
+                const int v = t[r * k + 5 * j + i];
+                if (v < -1 || v > 1) return ORC_BAD_VALUE;
+                b += (unsigned)(v + 1) * p;
+                p *= 3u;
+            }
+            codes[r * (k / 5) + j] = (uint8_t)b;
+        }
+    return ORC_OK;
+}
+
+int orc_unpack5(const uint8_t *codes, int64_t rows, int64_t k, int8_t *t)
+{
+    if (rows < 0 || k < 0 || k % 80 != 0) return ORC_BAD_SHAPE;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t j = 0; j < k / 5; ++j) {
+            unsigned b = codes[r * (k / 5) + j];
+            if (b > 242u) return ORC_BAD_CODE;
+            for (int i = 0; i < 5; ++i) {
+                t[r * k + 5 * j + i] = (int8_t)((int)(b % 3u) - 1);
+                b /= 3u;
+            }
+        }
+    return ORC_OK;
+}
+
+/* y[mi*rows + r] = scale[r] * sum_k t[r][k] * x[mi*k + k'] from base-3 codes,
+ * in double, for rows [row_begin, row_end). */
+int orc_gemm5(const uint8_t *codes, const float *scale, int64_t rows, int64_t k,
+              const uint16_t *x, int64_t m, double *y, int64_t row_begin, int64_t row_end)
+{
+    if (rows < 0 || k < 0 || k % 80 != 0 || m < 0) return ORC_BAD_SHAPE;
+    for (int64_t mi = 0; mi < m; ++mi)
+        for (int64_t r = row_begin; r < row_end; ++r) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < k / 5; ++j) {
+                unsigned b = codes[r * (k / 5) + j];
+                if (b > 242u) return ORC_BAD_CODE;
+                for (int i = 0; i < 5; ++i) {
+                    acc += (double)((int)(b % 3u) - 1) * orc_bf16_to_double(x[mi * k + 5 * j + i]);
+                    b /= 3u;
+                }
+            }
+            y[mi * rows + r] = (double)scale[r] * acc;
+        }
+    return ORC_OK;
+}
