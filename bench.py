@@ -241,12 +241,12 @@ def _graph_ms(fn, stream, reps: int, warm: int = 3) -> float:
 
 
 def extras(args, dev, stream, wl, peak):
-    """Three more measurements on rank 0, each never failing the bench line:
+    """More measurements on rank 0, each never failing the bench line:
     single_call (c1 as back-to-back tern_gemv launches in one graph, one
     launch per call), ordered_sweep (the 36-layer decode sweep as 4 launch
     groups per layer in dependency order, 144 tern_gemm_batched calls per
-    token) and lm_head (the 151,936 x 4,096 int8 output head with the fused
-    argmax, m = 1)."""
+    token), base3 (the 1.6-bit base-3 format on c1's rows) and lm_head (the
+    151,936 x 4,096 int8 output head with the fused argmax, m = 1)."""
     import torch
 
     import packed_bit_gemv_tern_b300 as tern
@@ -272,6 +272,26 @@ def extras(args, dev, stream, wl, peak):
         del keep
     except Exception as e:
         out["ordered_sweep"] = {"error": f"{type(e).__name__}: {e}"}
+    try:
+        # base-3 format: one tern5_gemv over 409,600 x 4,160 (c1's 100 x 4096
+        # rows, K padded to a multiple of 80), 341 MB of codes drawn uniformly
+        # over the valid bytes
+        rng = np.random.default_rng(555)
+        rows5, k5 = 409600, 4160
+        c5 = torch.from_numpy(rng.integers(0, 243, (rows5, k5 // 5), dtype=np.uint8)).to(dev)
+        s5 = torch.from_numpy(synth.scales(rng, rows5)).to(dev)
+        w5 = tern.Tern5Matrix(c5, s5, k5)
+        x5 = torch.from_numpy(synth.activations(rng, 1, k5).view(np.int16)).to(dev).view(torch.bfloat16)
+        y5 = torch.empty((1, rows5), dtype=torch.float32, device=dev)
+        ms = _graph_ms(lambda: tern.tern5_gemm(w5, x5, 1, y5, stream=stream), stream, reps=20)
+        gb = w5.packed_bytes / (ms * 1e-3) / 1e9
+        out["base3"] = {"workload": "base-3 codes (5 weights a byte), 409,600 x 4,160 at m = 1, one tern5_gemm",
+                        "us_per_call": round(1e3 * ms, 2), "gbs_codes": round(gb, 2), "frac": round(gb / peak, 4),
+                        "gweights_per_s": round(rows5 * k5 / (ms * 1e-3) / 1e9, 1),
+                        "two_bit_equivalent_gbs": round(rows5 * k5 / 4 / (ms * 1e-3) / 1e9, 2)}
+        del c5, w5
+    except Exception as e:
+        out["base3"] = {"error": f"{type(e).__name__}: {e}"}
     head = None
     try:
         rng = np.random.default_rng(777)
@@ -607,6 +627,7 @@ def run_ours(args, dist: Dist):
                    "graph": "one CUDA graph per step, replayed", "parallelism": f"replicas x{dist.world}",
                    "gpu": torch.cuda.get_device_name(dev), "spread": spread,
                    "single_call": more.get("single_call"), "ordered_sweep": more.get("ordered_sweep"),
+                   "base3": more.get("base3"),
                    "api": (f"tern_gemm_batched: {main_launches} persistent launch(es) per step"
                            + (f" and {prep_launches} activation-preparing launch(es)" if prep_launches else "")
                            if args.api == "batched" else "one tern_* launch per call")},

@@ -76,7 +76,7 @@
 extern "C" {
 #endif
 
-#define TERN_ABI_VERSION 1
+#define TERN_ABI_VERSION 2
 
 /* Exported symbols (the library is built with hidden default visibility). */
 #if defined(__GNUC__)
@@ -303,6 +303,40 @@ typedef struct {
 TERN_API tern_status tern_lmhead_argmax(const tern_i8_matrix *w, const uint16_t *x, int32_t m,
                                         const float *norm_w, float eps, float *logits, int32_t *argmax,
                                         void *stream);
+
+/* A denser packing: five ternary weights per byte, 1.6 bits a weight (the
+ * model page's byte budget, "Where the bytes live", spends more bits per
+ * weight than a ternary value needs; this format is the library's own):
+ *   - K must be a multiple of 80 (pad rows with zero weights);
+ *   - codes: R * K/5 bytes, row-major; byte j of a row holds weights
+ *     5j .. 5j+4 as b = sum_{i<5} (t_{5j+i} + 1) * 3^i (least significant
+ *     digit first), b in [0, 242]; 243..255 are invalid: tern5_pack never
+ *     writes them and the device kernels give an unspecified (but fault-free)
+ *     result for them (tern5_unpack writes -2);
+ *   - scale: R fp32, applied after the sum.
+ * codes: 16-byte aligned; scale: 4-byte aligned. */
+typedef struct {
+    int32_t rows;          /* R >= 0 */
+    int32_t k;             /* K >= 0, K % 80 == 0 */
+    const uint8_t *codes;  /* R * K/5 */
+    const float *scale;    /* R */
+} tern5_matrix;
+
+/* Pack an int8 matrix t [rows][k] (values -1, 0, +1; k % 80 == 0) into
+ * base-3 codes [rows][k/5] and write rowsum[rows] (may be NULL).  Host
+ * memory, synchronous.  Errors: TERN_ERR_NULL, TERN_ERR_SHAPE,
+ * TERN_ERR_VALUE. */
+TERN_API tern_status tern5_pack(const int8_t *t, int32_t rows, int32_t k, uint8_t *codes, int32_t *rowsum);
+
+/* Decode base-3 codes to int8 t_out [rows][k] on the device (bit-exact). */
+TERN_API tern_status tern5_unpack(const tern5_matrix *w, int8_t *t_out, void *stream);
+
+/* y[i][r] = scale[r] * sum_k t[r][k] x[i][k], i < m, from base-3 codes, on
+ * the CUDA cores (each byte's five digits by division by 3 as a multiply
+ * and shift; fp32 accumulation).  x: [m][k] bf16, 16-byte aligned; y:
+ * [m][rows] fp32.  1 <= m <= TERN_MAX_M, m * k * 2 <= TERN_MAX_X_BYTES.
+ * One launch; allocates nothing.  Errors as tern_gemm_smallm. */
+TERN_API tern_status tern5_gemm(const tern5_matrix *w, const uint16_t *x, int32_t m, float *y, void *stream);
 
 /* Synchronise `stream`, then report and clear the device error word that
  * bounded device-side waits set when they run out (TERN_ERR_TIMEOUT), or a

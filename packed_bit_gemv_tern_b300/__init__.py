@@ -39,6 +39,7 @@ ABI_FUNCTIONS = (
     "tern_pack", "tern_validate", "tern_unpack", "tern_gemv", "tern_gemv_swiglu",
     "tern_gemm_smallm", "tern_gemm_smallm_swiglu", "tern_gemm_batched", "tern_gemm_batched_launches",
     "tern_gemm_batched_noalloc", "tern_gemm_batched_rmsnorm", "tern_lmhead_argmax",
+    "tern5_pack", "tern5_unpack", "tern5_gemm",
     "tern_last_device_error", "tern_set_wait_limit",
     "tern_status_str", "tern_abi_version",
 )
@@ -57,6 +58,11 @@ class CMatrix(ctypes.Structure):
 
 class CI8Matrix(ctypes.Structure):
     _fields_ = [("rows", ctypes.c_int32), ("k", ctypes.c_int32), ("w", ctypes.c_void_p), ("scale", ctypes.c_void_p)]
+
+
+class C5Matrix(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int32), ("k", ctypes.c_int32), ("codes", ctypes.c_void_p),
+                ("scale", ctypes.c_void_p)]
 
 
 class CBatchItem(ctypes.Structure):
@@ -93,6 +99,9 @@ def load(path: str | None = None):
             "tern_gemm_batched_noalloc": [vp, i32, vp],
             "tern_gemm_batched_rmsnorm": [vp, vp, ctypes.c_float, i32, vp],
             "tern_lmhead_argmax": [vp, vp, i32, vp, ctypes.c_float, vp, vp, vp],
+            "tern5_pack": [vp, i32, i32, vp, vp],
+            "tern5_unpack": [vp, vp, vp],
+            "tern5_gemm": [vp, vp, i32, vp, vp],
             "tern_last_device_error": [vp],
             "tern_set_wait_limit": [ctypes.c_int64],
             "tern_status_str": [ctypes.c_int],
@@ -206,6 +215,48 @@ class I8Matrix:
 
     def ref(self):
         return ctypes.byref(self._c)
+
+
+class Tern5Matrix:
+    """A base-3 packed matrix (five weights per byte) resident on the GPU."""
+
+    def __init__(self, codes, scale, k: int):
+        self.codes = codes    # torch.uint8 [rows, k//5]
+        self.scale = scale    # torch.float32 [rows]
+        self.rows, self.k = int(scale.shape[0]), int(k)
+        self._c = C5Matrix(self.rows, self.k, codes.data_ptr() if codes.numel() else None,
+                           scale.data_ptr() if scale.numel() else None)
+
+    @classmethod
+    def from_host(cls, codes: np.ndarray, scale: np.ndarray, k: int, device="cuda"):
+        import torch
+        return cls(torch.from_numpy(np.ascontiguousarray(codes, np.uint8)).to(device),
+                   torch.from_numpy(np.ascontiguousarray(scale, np.float32)).to(device), k)
+
+    @property
+    def packed_bytes(self) -> int:
+        return self.rows * self.k // 5
+
+    def ref(self):
+        return ctypes.byref(self._c)
+
+
+def tern5_pack(t: np.ndarray):
+    """int8 [rows, k] (k % 80 == 0) -> (uint8 codes [rows, k//5], int32 rowsum [rows])."""
+    t = np.ascontiguousarray(t, dtype=np.int8)
+    rows, k = t.shape
+    codes = np.zeros((rows, k // 5), dtype=np.uint8)
+    rowsum = np.zeros(rows, dtype=np.int32)
+    _check(load().tern5_pack(_np_ptr(t), rows, k, _np_ptr(codes), _np_ptr(rowsum)), "tern5_pack")
+    return codes, rowsum
+
+
+def tern5_unpack(w: "Tern5Matrix", t_out, stream=None):
+    _check(load().tern5_unpack(w.ref(), _dptr(t_out), _stream_handle(stream)), "tern5_unpack")
+
+
+def tern5_gemm(w: "Tern5Matrix", x, m: int, y, stream=None):
+    _check(load().tern5_gemm(w.ref(), _dptr(x), int(m), _dptr(y), _stream_handle(stream)), "tern5_gemm")
 
 
 def _stream_handle(stream):

@@ -239,6 +239,42 @@ extern "C" tern_status tern_gemm_batched_rmsnorm(const tern_batch_item *items, c
     return gemm_batched_rmsnorm(items, norm_w, eps, n, (cudaStream_t)stream);
 }
 
+// Checks of a base-3 matrix: shape, pointers, alignment (codes 16 bytes).
+static tern_status check5(const tern5_matrix *w)
+{
+    if (w == nullptr) return TERN_ERR_NULL;
+    if (w->rows < 0 || w->k < 0 || w->k % 80 != 0) return TERN_ERR_SHAPE;
+    if (w->rows == 0 || w->k == 0) return TERN_OK;
+    if (w->codes == nullptr || w->scale == nullptr) return TERN_ERR_NULL;
+    if (!aligned(w->codes, 16) || !aligned(w->scale, 4)) return TERN_ERR_ALIGN;
+    return TERN_OK;
+}
+
+extern "C" tern_status tern5_gemm(const tern5_matrix *w, const uint16_t *x, int32_t m, float *y, void *stream)
+{
+    tern_status st = check5(w);
+    if (st != TERN_OK) return st;
+    if (m < 1 || m > TERN_MAX_M) return TERN_ERR_M_RANGE;
+    if (w->rows == 0) return TERN_OK;
+    if ((int64_t)m * w->k * 2 > TERN_MAX_X_BYTES) return TERN_ERR_SHAPE;
+    if (x == nullptr || y == nullptr) return TERN_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(y, 4)) return TERN_ERR_ALIGN;
+    if (w->k == 0) {  // y = scale * 0
+        const tern_matrix z = {w->rows, 0, nullptr, w->scale, nullptr};
+        return empty_sum(&z, nullptr, m, y, (cudaStream_t)stream);
+    }
+    return tern5_gemm_launch(w, x, m, y, (cudaStream_t)stream);
+}
+
+extern "C" tern_status tern5_unpack(const tern5_matrix *w, int8_t *t_out, void *stream)
+{
+    const tern_status st = check5(w);
+    if (st != TERN_OK) return st;
+    if (w->rows == 0 || w->k == 0) return TERN_OK;
+    if (t_out == nullptr) return TERN_ERR_NULL;
+    return tern5_unpack_launch(w, t_out, (cudaStream_t)stream);
+}
+
 extern "C" tern_status tern_lmhead_argmax(const tern_i8_matrix *w, const uint16_t *x, int32_t m, const float *norm_w,
                                           float eps, float *logits, int32_t *argmax, void *stream)
 {

@@ -52,6 +52,35 @@ extern "C" tern_status tern_pack(const int8_t *t, int32_t rows, int32_t k,
     return TERN_OK;
 }
 
+extern "C" tern_status tern5_pack(const int8_t *t, int32_t rows, int32_t k, uint8_t *codes, int32_t *rowsum)
+{
+    if (rows < 0 || k < 0 || (k % 80) != 0) return TERN_ERR_SHAPE;
+    if (rows == 0 || k == 0) {
+        if (rowsum != nullptr)
+            for (int32_t r = 0; r < rows; ++r) rowsum[r] = 0;
+        return TERN_OK;
+    }
+    if (t == nullptr || codes == nullptr) return TERN_ERR_NULL;
+    const int64_t bpr = k / 5;
+    for (int64_t r = 0; r < rows; ++r) {
+        const int8_t *src = t + r * (int64_t)k;
+        int64_t sum = 0;
+        for (int64_t j = 0; j < bpr; ++j) {
+            // Horner from the most significant digit: b = sum_i (t_i + 1) 3^i
+            uint32_t b = 0;
+            for (int i = 4; i >= 0; --i) {
+                const int8_t v = src[5 * j + i];
+                if (!is_ternary(v)) return TERN_ERR_VALUE;
+                b = 3u * b + (uint32_t)(v + 1);
+                sum += v;
+            }
+            codes[r * bpr + j] = (uint8_t)b;
+        }
+        if (rowsum != nullptr) rowsum[r] = (int32_t)sum;
+    }
+    return TERN_OK;
+}
+
 extern "C" tern_status tern_validate(const uint32_t *codes, int32_t rows, int32_t k,
                                      const int32_t *rowsum, int64_t counts_out[3])
 {

@@ -32,6 +32,9 @@ tern_status take_mma_error();
 // Number of kernel launches gemm_batched makes for these items (host only).
 int batched_launches(const tern_batch_item *items, int n);
 tern_status gemm_batched(const tern_batch_item *items, int n, cudaStream_t s);
+// Base-3 products and unpack (arguments checked by the caller).
+tern_status tern5_gemm_launch(const tern5_matrix *w, const uint16_t *x, int m, float *y, cudaStream_t s);
+tern_status tern5_unpack_launch(const tern5_matrix *w, int8_t *t, cudaStream_t s);
 // int8 head logits and per-row argmax (arguments checked by the caller).
 tern_status head_argmax(const tern_i8_matrix *w, const uint16_t *x, int m, const float *norm_w, float eps,
                         float *logits, int32_t *argmax, cudaStream_t s);

@@ -21,7 +21,7 @@ def _declared():
     for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
         if fn.endswith(".h"):
             src = open(os.path.join(ROOT, "include", fn)).read()
-            names += re.findall(r"^TERN_API[^(]*?\b(tern_\w+)\s*\(", src, flags=re.M)
+            names += re.findall(r"^TERN_API[^(]*?\b(tern\d*_\w+)\s*\(", src, flags=re.M)
     return names
 
 
@@ -38,7 +38,7 @@ def test_exports_every_declared_symbol(lib):
     for n in names:
         assert hasattr(lib, n), n
     assert set(tern.ABI_FUNCTIONS) <= set(names)
-    assert tern.tern_abi_version() == 1
+    assert tern.tern_abi_version() == 2
 
 
 def test_header_constants_match_binding():
@@ -175,6 +175,18 @@ def test_device_entry_points_reject_before_launch(lib):
     arr[1].m = 9  # a bad item is reported before the norm arguments
     assert f(pa, None, ctypes.c_float(-1.0), 2, None) == tern.TERN_ERR_M_RANGE
     arr[1].m = 1
+    # base-3 format: shape, pointers and alignment before a launch
+    c5 = tern.C5Matrix(4, 160, 0x7000, 0x7100)
+    assert lib.tern5_gemm(None, x, 1, y, None) == tern.TERN_ERR_NULL
+    assert lib.tern5_gemm(ref(tern.C5Matrix(4, 150, 0x7000, 0x7100)), x, 1, y, None) == tern.TERN_ERR_SHAPE
+    assert lib.tern5_gemm(ref(c5), x, 0, y, None) == tern.TERN_ERR_M_RANGE
+    assert lib.tern5_gemm(ref(c5), x, 9, y, None) == tern.TERN_ERR_M_RANGE
+    assert lib.tern5_gemm(ref(tern.C5Matrix(4, 160, 0x7008, 0x7100)), x, 1, y, None) == tern.TERN_ERR_ALIGN
+    assert lib.tern5_gemm(ref(c5), ctypes.c_void_p(0x3008), 1, y, None) == tern.TERN_ERR_ALIGN
+    assert lib.tern5_gemm(ref(c5), x, 1, None, None) == tern.TERN_ERR_NULL
+    assert lib.tern5_gemm(ref(tern.C5Matrix(4, 24640, 0x7000, 0x7100)), x, 4, y, None) == tern.TERN_ERR_SHAPE
+    assert lib.tern5_unpack(ref(c5), None, None) == tern.TERN_ERR_NULL
+    assert lib.tern5_gemm(ref(tern.C5Matrix(0, 160, None, None)), None, 1, None, None) == tern.TERN_OK
     # int8 head: every argument is checked before a launch
     h = tern.CI8Matrix(10, 128, 0x7000, 0x7100)
     lg, am = ctypes.c_void_p(0x8000), ctypes.c_void_p(0x9000)
@@ -232,3 +244,23 @@ def test_batched_launch_plan(lib):
     assert lib.tern_gemm_batched_launches(None, 0) == 0
     assert lib.tern_gemm_batched_launches(None, 3) == -tern.TERN_ERR_NULL
     assert lib.tern_gemm_batched_launches(None, -1) == -tern.TERN_ERR_SHAPE
+
+
+@pytest.mark.parametrize("rows,k,seed", [(1, 80, 0), (7, 400, 1), (33, 4160, 2)])
+def test_base3_pack_matches_oracle_encoder(lib, rows, k, seed):
+    rng = np.random.default_rng(seed)
+    t = synth.ternary(rng, rows, k)
+    codes, rowsum = tern.tern5_pack(t)
+    assert np.array_equal(codes, oracle.pack5(t))
+    assert np.array_equal(rowsum, t.astype(np.int64).sum(axis=1))
+
+
+def test_base3_pack_rejects(lib):
+    with pytest.raises(tern.TernError) as e:
+        tern.tern5_pack(np.zeros((2, 64), dtype=np.int8))
+    assert e.value.status == tern.TERN_ERR_SHAPE
+    bad = np.zeros((1, 80), dtype=np.int8)
+    bad[0, 17] = 2
+    with pytest.raises(tern.TernError) as e:
+        tern.tern5_pack(bad)
+    assert e.value.status == tern.TERN_ERR_VALUE
