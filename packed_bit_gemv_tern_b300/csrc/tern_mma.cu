@@ -246,27 +246,44 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
                 }
             }
         };
-        for (int first = st_tid; first < n_items; first += kStagers * kStageItems) {  // max |x| per row
+        // The two statistics passes reduce within each warp first and make one
+        // shared-memory atomic per warp: a warp's 32 items at a given t are 32
+        // consecutive words of one activation row (n_words is a multiple of
+        // 32), and every thread takes the same number of turns, past n_items
+        // with zeros.
+        for (int base_i = 0; base_i < n_items; base_i += kStagers * kStageItems) {  // max |x| per row
+            const int first = base_i + st_tid;
             load_batch(first);
 #pragma unroll
             for (int t = 0; t < kStageItems; ++t) {
                 const int item = first + t * kStagers;
-                if (item < n_items) atomicMax(&xmax[2 * (item / n_words)], max_abs16(xa[t], xb[t]));
+                const uint32_t v = __reduce_max_sync(0xFFFFFFFFu, item < n_items ? max_abs16(xa[t], xb[t]) : 0u);
+                const int item0 = item - lane;
+                if (lane == 0 && item0 < n_items) atomicMax(&xmax[2 * (item0 / n_words)], v);
             }
         }
         ptx::named_bar_sync(3, kStagers);
-        for (int first = st_tid; first < n_items; first += kStagers * kStageItems) {  // band B of each row
+        for (int base_i = 0; base_i < n_items; base_i += kStagers * kStageItems) {  // band B of each row
+            const int first = base_i + st_tid;
             if (!resident) load_batch(first);
 #pragma unroll
             for (int t = 0; t < kStageItems; ++t) {
                 const int item = first + t * kStagers;
+                const int item0 = item - lane;
+                const int mm = item0 < n_items ? item0 / n_words : 0;
+                const uint32_t tb2 = band_threshold2(xmax[2 * mm]);
+                uint32_t n = 0, mb = 0;
+                float sabs = 0.f;
                 if (item < n_items) {
-                    const int mm = item / n_words;
-                    const uint32_t tb2 = band_threshold2(xmax[2 * mm]);
-                    uint32_t n = 0;
-                    float sabs = 0.f;
                     band_stats16(xa[t], xb[t], tb2, n, sabs);
-                    atomicMax(&xmax[2 * mm + 1], max_abs16_below(xa[t], xb[t], tb2));
+                    mb = max_abs16_below(xa[t], xb[t], tb2);
+                }
+                mb = __reduce_max_sync(0xFFFFFFFFu, mb);
+                n = __reduce_add_sync(0xFFFFFFFFu, n);
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) sabs += __shfl_xor_sync(0xFFFFFFFFu, sabs, o);
+                if (lane == 0 && item0 < n_items) {
+                    atomicMax(&xmax[2 * mm + 1], mb);
                     atomicAdd(&n_small[mm], n);
                     atomicAdd(&sum_abs[mm], sabs);
                 }
@@ -373,9 +390,9 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
     // the epilogue reads them.
     __syncwarp();
     __syncthreads();
-    // per activation row, this rank's sum as an unevaluated pair (acc_pair):
-    // its bands, and then the ranks' partials, may cancel at very different
-    // magnitudes
+    // per activation row, this rank's sum: plain fp32 with one band, an
+    // unevaluated pair (acc_pair) with two, whose terms, and then the ranks'
+    // partials, may cancel at very different magnitudes
     float acc[8], acc_lo[8];
 #pragma unroll
     for (int n = 0; n < 8; ++n) acc[n] = acc_lo[n] = 0.f;
@@ -408,12 +425,13 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
             if (bands == 1) {  // column 2i + b of row i: hi, lo
                 float dsum[16];
                 sum_group(0u, dsum);
+                // one band: each row's sum is within 2^-24 of its sum |x|
+                // already, so it stays a plain fp32 sum (acc_lo stays zero)
 #pragma unroll
                 for (int mm = 0; mm < 8; ++mm) {
                     if (mm < m) {
                         const int sa = row_scale_exp(xmax[2 * mm]);
-                        acc_pair(acc[mm], acc_lo[mm], dsum[2 * mm] * exp2i(-sa));
-                        acc_pair(acc[mm], acc_lo[mm], dsum[2 * mm + 1] * exp2i(-sa - 4));
+                        acc[mm] = fmaf(dsum[2 * mm + 1], exp2i(-sa - 4), dsum[2 * mm] * exp2i(-sa));
                     }
                 }
             } else {  // column 4i + b of row i: hi_A, lo_A, hi_B, lo_B
@@ -453,12 +471,25 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
         if (epi && rank == 0) {
 #pragma unroll
             for (int n = 0; n < 8; ++n) acc[n] = acc_lo[n] = 0.f;
+            // plain fp32 adds while every rank had one band (its lo parts
+            // are zero); exact pairs once a rank took two
+            bool pairs = false;
             for (int r = 0; r < split; ++r) {
                 const float *v = red + ((size_t)r * 128 + i) * 16;
 #pragma unroll
-                for (int n = 0; n < 8; ++n) {
-                    acc_pair(acc[n], acc_lo[n], v[n]);
-                    acc_pair(acc[n], acc_lo[n], v[8 + n]);
+                for (int n = 0; n < 8; ++n) pairs = pairs || v[8 + n] != 0.f;
+            }
+            for (int r = 0; r < split; ++r) {
+                const float *v = red + ((size_t)r * 128 + i) * 16;
+                if (pairs) {
+#pragma unroll
+                    for (int n = 0; n < 8; ++n) {
+                        acc_pair(acc[n], acc_lo[n], v[n]);
+                        acc_pair(acc[n], acc_lo[n], v[8 + n]);
+                    }
+                } else {
+#pragma unroll
+                    for (int n = 0; n < 8; ++n) acc[n] += v[n];
                 }
             }
         }
