@@ -1,39 +1,48 @@
 // tern_batched.cu -- one persistent launch for a batch of independent ternary
 // products: M = 1 GEMVs, small-M GEMMs and fused SwiGLU pairs (Neutrino-1 8B
 // model page: seven coded linears per layer, gate/up feeding a SwiGLU; the
-// speculative verifier's M = 7 pass).
+// speculative verifier's M = 7 pass), optionally behind an RMSNorm of their
+// activations (spec table); and, as a second instantiation of the same
+// kernel, the int8 output head with the greedy argmax fused ("Where the
+// bytes live"; the spec-decode paragraph's greedy acceptance).
 //
 // Each of the grid's CTAs (one per SM) owns a contiguous run of work units;
 // a unit is one 128-row tile (64 gate + 64 up rows for a SwiGLU pair) of one
 // item over the item's whole K, so no unit needs a cross-CTA reduction.  The
-// host balances the runs by packed bytes.  K is processed in chunks of up to
-// 14336 / m codes (the whole K for m = 1 at every Neutrino shape); the B
-// operand (each activation as four e4m3 terms in two magnitude bands under
-// per-row power-of-two scales per chunk, see split_word2) and the fp32
-// accumulators are double buffered per chunk; a chunk's B is reused by every
-// later tile of the item on the same buffer, and fetching
-// the next chunk's B and reading the previous chunk's sums overlap the weight
-// stream.  Roles (17 warps):
+// host balances the runs by packed bytes.  K is processed in chunks whose
+// one-band B fits a 56 KB buffer (the whole K for m = 1 at every Neutrino
+// shape).  The B operand holds each activation as two e4m3 terms (hi, lo)
+// under a per-row power-of-two scale per chunk; a chunk where small
+// elements would matter (outlier channels) takes two magnitude bands, four
+// terms, across both buffers (split_word2).  B and the fp32 accumulators
+// are double buffered per chunk; a one-band chunk's B is reused by every
+// later tile of the item on the same buffer, and fetching the next chunk's
+// B and reading the previous chunk's sums overlap the weight stream.
+// Roles (17 warps):
 //   * warp 0, lane 0: TMA producer; streams every stage of every unit of the
-//     CTA through a 6-deep ring of 16 KB stages (128 rows x 512 codes,
-//     128-byte swizzle), never waiting on activations.
+//     CTA through a 6-deep ring of 16 KB stages (128 rows x 512 codes, or
+//     x 128 int8 weights; 128-byte swizzle), never waiting on activations.
 //   * warps 1-4: bring in B for each chunk (after griddepcontrol.wait), then
 //     read the previous chunk's accumulators, rescale and add them into
-//     per-row registers, and at the end of a unit write y (scale, SiLU gate).
-//     For m = 1 they build B from x themselves; for m >= 2 a short kernel
-//     launched just before (k_tern_bprep) has written every chunk's B and row
-//     maxima to a workspace once, and a chunk is one bulk copy: building it
-//     in every CTA that streams a tile of the item costs more than the
-//     chunk's weight stream when m is large.
+//     per-row registers, and at the end of a unit write y (scale, SiLU gate;
+//     int8 head: logits and the argmax keys).  For m = 1 they build B from x
+//     themselves (normalising it first for items with a norm); for m >= 2 a
+//     short kernel launched just before (k_tern_bprep) has written every
+//     chunk's one-band B, row maxima and band flags to a workspace once, and
+//     a one-band chunk is one bulk copy: building it in every CTA that
+//     streams a tile of the item costs more than the chunk's weight stream
+//     when m is large.
 //   * warps 5-16: three decoder groups of four warps; group g turns the four
 //     chunk columns (128 codes of a row each) of the stages s = g (mod 3)
 //     into e4m3 +-2/0 bytes (decode8) in TMEM slot g, and lane 0 of warp q
-//     of the group then issues the K=32 steps of column q (tcgen05.mma
+//     of the group then issues the K = 32 steps of column q (tcgen05.mma
 //     kind::f8f6f4, A from TMEM, B from shared memory, M = 128) into the
-//     column's accumulator of the chunk's buffer: four columns of 128 codes
-//     at N = 16 (m <= 4), or two of 256 codes issued by warps 0 and 1 at
-//     N = 32 (m >= 5), so both fit the same 128 accumulator columns.  Three decoder warps
-//     per scheduler hide each other's barrier latency.
+//     column's accumulator of the chunk's buffer.  One-band chunks take the
+//     fixed N = 16 path; two-band chunks an out-of-line one (N = 16 for
+//     m <= 4; N = 32 for m >= 5 as two 256-code columns from quads 0 and
+//     1).  Three decoder warps per scheduler hide each other's barrier
+//     latency.  The int8 format decodes each weight into two exact e4m3
+//     nibbles and issues one MMA per nibble and K step (see kFmtI8).
 // Every mbarrier wait is bounded; on time-out the kernel records the error,
 // stops, drains its copies and MMAs, releases its tensor memory and returns.
 #include <cuda.h>
