@@ -299,13 +299,18 @@ __global__ void __launch_bounds__(kPrepThreads) k_tern_bprep(const __grid_consta
     const int w0 = c * it.cstages * it.sw;
     const int nw = min(it.cstages, it.stages - c * it.cstages) * it.sw;
     const int kw = it.k / 16;
+    // Word slots a thread uses: every loop over the slots stops at nq (the
+    // same for the whole CTA), so a chunk shorter than the largest one runs
+    // only the code of its own slots.  Each CTA passes through the code once,
+    // so the instructions it executes are mostly fetched cold.
+    const int nq = (nw + kPrepThreads - 1) / kPrepThreads;
     const uint4 *xr = reinterpret_cast<const uint4 *>(it.x + (size_t)mm * it.k);  // 2 x uint4 per word
     uint4 va[kPrepWords], vb[kPrepWords];
 #pragma unroll
     for (int q = 0; q < kPrepWords; ++q) {
         const int wi = tid + q * kPrepThreads, gw = w0 + wi;
         va[q] = vb[q] = make_uint4(0u, 0u, 0u, 0u);
-        if (wi < nw && gw < kw) {
+        if (q < nq && wi < nw && gw < kw) {
             va[q] = __ldg(xr + 2 * gw);
             vb[q] = __ldg(xr + 2 * gw + 1);
         }
@@ -327,19 +332,24 @@ __global__ void __launch_bounds__(kPrepThreads) k_tern_bprep(const __grid_consta
         const float4 *g4 = reinterpret_cast<const float4 *>(it.norm_w);
 #pragma unroll
         for (int q = 0; q < kPrepWords; ++q) {
+            if (q >= nq) break;
             const int wi = tid + q * kPrepThreads, gw = w0 + wi;
             if (wi < nw && gw < kw) rmsnorm_word(va[q], vb[q], g4 + 4 * gw, rn);
         }
     }
     uint32_t mx = 0;
 #pragma unroll
-    for (int q = 0; q < kPrepWords; ++q) mx = max(mx, max_abs16(va[q], vb[q]));
+    for (int q = 0; q < kPrepWords; ++q) {
+        if (q >= nq) break;
+        mx = max(mx, max_abs16(va[q], vb[q]));
+    }
     const uint32_t ma = prep_cta_max(mx, red);
     const uint32_t tb2 = band_threshold2(ma);
     uint32_t n = 0, mb = 0;
     float sabs = 0.f;
 #pragma unroll
     for (int q = 0; q < kPrepWords; ++q) {
+        if (q >= nq) break;
         band_stats16(va[q], vb[q], tb2, n, sabs);
         mb = max(mb, max_abs16_below(va[q], vb[q], tb2));
     }
@@ -365,7 +375,10 @@ __global__ void __launch_bounds__(kPrepThreads) k_tern_bprep(const __grid_consta
     if (it.head) {
         double sx = 0.0;
 #pragma unroll
-        for (int q = 0; q < kPrepWords; ++q) sx += sum16(va[q], vb[q]);
+        for (int q = 0; q < kPrepWords; ++q) {
+            if (q >= nq) break;
+            sx += sum16(va[q], vb[q]);
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) sx += __shfl_xor_sync(0xFFFFFFFFu, sx, o);
         __syncthreads();  // ssred free
@@ -392,6 +405,7 @@ __global__ void __launch_bounds__(kPrepThreads) k_tern_bprep(const __grid_consta
     unsigned char *dst = it.b + (size_t)w0 * wbytes + 32u * (size_t)mm;
 #pragma unroll
     for (int q = 0; q < kPrepWords; ++q) {
+        if (q >= nq) break;
         const int wi = tid + q * kPrepThreads;
         if (wi < nw) {
             uint4 rows[2];
