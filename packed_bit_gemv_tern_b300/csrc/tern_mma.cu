@@ -121,7 +121,9 @@ constexpr uint32_t kBarBytes = kWords + kWordsCount * 4;
 
 using namespace mma;
 
-template <bool SWIGLU>
+// kStageItems: activation words a staging thread takes per batch (see the
+// staging warps).
+template <bool SWIGLU, int kStageItems>
 __global__ void __launch_bounds__(kThreads, 1)
 k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_u, const MmaParams p)
 {
@@ -225,8 +227,10 @@ k_tern_mma(const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUt
         // Items are processed in batches of kStageItems per thread: all loads of
         // a batch are issued before any is used, so a batch costs one memory
         // latency.  Small problems (n_items <= kStagers * kStageItems) keep
-        // their activations in registers across the three passes.
-        constexpr int kStageItems = 4;
+        // their activations in registers across the three passes.  The host
+        // takes kStageItems = 1 when every item of the CTA fits one batch of
+        // one per thread, else 4: each pass then runs a quarter of the code,
+        // which a CTA executes once, with cold instruction caches.
         uint4 xa[kStageItems], xb[kStageItems];
         const bool resident = n_items <= kStagers * kStageItems;
         auto load_batch = [&](int first) {
@@ -548,8 +552,15 @@ tern_status launch_mma(const tern_matrix *g, const tern_matrix *u, const uint16_
     const int total_st = (kw + kStageWords - 1) / kStageWords;
     const int sms = sm_count();
 
+    // Split K over a cluster while the CTAs still fit the SMs and each rank
+    // keeps at least four stages.  Measured one call at a time on the
+    // decode shapes: 1024x4096 at split 2 / 4 / 8 took 7.7 / 8.3 / 11.3 us,
+    // 4096x4096 at 2 / 4 took 8.0 / 9.0 us, and the 4096x12288 down
+    // projection ran faster at 4 than at 2.  Each rank pays its own prologue,
+    // statistics passes and cluster exchange; below four stages that costs
+    // more than the wider weight stream gains.
     int split = 1;
-    while (split < 8 && tiles * split * 2 <= sms && split * 2 <= total_st) split *= 2;
+    while (split < 8 && tiles * split * 2 <= sms && split * 2 * 4 <= total_st) split *= 2;
     const uint32_t wbytes = b_block_bytes(m, 2);  // room for two bands
     int per_st = 0, n_wst = 0;
     for (;;) {
@@ -597,7 +608,10 @@ tern_status launch_mma(const tern_matrix *g, const tern_matrix *u, const uint16_
         if (SWIGLU && !make_code_map(&tu, u->codes, rows, kw, tile_rows)) return TERN_ERR_CUDA;
     }
 
-    auto kern = k_tern_mma<SWIGLU>;
+    // staging batch: one activation word per thread when a CTA's words (its
+    // K range, every activation row) fit the staging threads once
+    const bool one_item = (long long)m * per_st * kStageWords <= kStagers;
+    auto kern = one_item ? k_tern_mma<SWIGLU, 1> : k_tern_mma<SWIGLU, 4>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
         return TERN_ERR_CUDA;
 
